@@ -1,0 +1,386 @@
+"""Benchmark of the split-KV attention forward on GB300.
+
+One step = one sk_attn_fwd over the workload (split counts -> partial kernel ->
+combine), inputs resident in HBM. Default workload: the long-context varlen
+prefill target shape (bf16, Sq 4096, Sk 42700, H 12, D_QK 192, D_V 128,
+non-causal, split_kv automatic -> 3). Inputs (347 MB) are larger than L2.
+
+Prints one JSON line. Besides the step throughput it reports, measured live:
+  roofline      the partial kernel's TFLOP/s (CUDA events on its stream) against
+                the measured dense bf16 peak, plus ncu DRAM traffic from profiles/
+  combine       the combine kernel's HBM GB/s (L2 flushed before each launch)
+  e2e           the same metric through the public call with host buffers and
+                host<->device copies inside the timed region
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+  clocks        nvidia-smi samples taken during the timed work
+
+--impl reference times the CPU oracle as the reference arm (rank 0 only).
+Multi-GPU (torchrun): every rank runs the same workload (replicas, weak scaling),
+barrier + max-over-ranks timing, value = all ranks' FLOPs / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from split_kv_attention_flash_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "split-KV attn fwd TFLOP/s (bf16, Sq4096 Sk42.7K H12); combine HBM GB/s"
+UNIT = "TFLOP/s"
+# The pages' split-3 time on MI325X for this exact shape (2.269 ms) as TFLOP/s.
+PAGES_SPLIT3_TFLOPS = 2 * 4096 * 42700 * 12 * (192 + 128) / 2.269e-3 / 1e12
+L2_BYTES = 129 * 1024 * 1024
+
+
+def flops_of(w, rows=None) -> float:
+    """4 * Sq * Sk_visible * H * (D_QK + D_V) / 2 over visible (row, key) pairs."""
+    total = 0
+    for b in range(w.B):
+        sq, sk = w.seqlens_q[b], w.seqlens_k[b]
+        last = sk - 1 if w.last_valid_kv_index < 0 else min(w.last_valid_kv_index, sk - 1)
+        qs = np.arange(sq) if rows is None else np.asarray(
+            [r - w.cu_seqlens_q[b] for r in rows if w.cu_seqlens_q[b] <= r < w.cu_seqlens_q[b + 1]])
+        if len(qs) == 0:
+            continue
+        if w.mask == wl.MASK_NONE:
+            vis = np.full(len(qs), last + 1)
+        else:
+            off = w.prefix_offset if w.mask == wl.MASK_PREFIX_CAUSAL else 0
+            vis = np.clip(np.minimum(qs + off, last) + 1, 0, None)
+        total += int(vis.sum())
+    return 2.0 * total * w.H * (w.d_qk + w.d_v)
+
+
+def combine_bytes(w, counts: np.ndarray, with_lse: bool) -> float:
+    es = 2 if w.dtype != "f32" else 4
+    per_row = counts.astype(np.int64) * (4 * w.d_v + 4) + w.d_v * es + (4 if with_lse else 0)
+    return float(per_row.sum() * w.H + 4 * w.total_q)
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm": d["hbm_gbs"], "bf16": d["bf16_tflops"],
+                "bf16_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, valid only while the
+    kernel's source file is unchanged (its sha256 is recorded beside the number)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") != kernel or "source" not in f:
+            continue
+        src = os.path.join(ROOT, f["source"])
+        if not os.path.exists(src):
+            continue
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != f.get("sha256"):
+            return None
+        return float(f["dram_bytes_per_launch"]) * float(f.get("scale", 1.0))
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[4]), f[5:9]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] >= 50] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(loaded)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def time_oracle(w, target_s: float, seed: int = 0, inputs=None):
+    """The oracle, as it is, on a bounded random sample of rows (all heads)."""
+    import oracle
+    q, k, v = inputs if inputs is not None else w.make_inputs("cpu")
+    prob = oracle.Problem(cu_q=w.cu_seqlens_q, cu_k=w.cu_seqlens_k, H=w.H, d_qk=w.d_qk,
+                          d_v=w.d_v, mask=w.mask, prefix_offset=w.prefix_offset,
+                          last_valid_kv_index=w.last_valid_kv_index, n_per_block=w.n_per_block)
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(seed)
+    n = max(cores, 16)
+    rows = np.sort(rng.choice(w.total_q, size=n, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention(prob, q, k, v, rows=rows, nthreads=cores)
+    dt = time.perf_counter() - t0
+    n2 = int(min(w.total_q, max(n, n * target_s / max(dt, 1e-3))))
+    n2 = max(cores, (n2 // cores) * cores)
+    rows = np.sort(rng.choice(w.total_q, size=n2, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention(prob, q, k, v, rows=rows, nthreads=cores)
+    dt = time.perf_counter() - t0
+    fl = flops_of(w, rows.tolist())
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n2} random query rows x {w.H} heads of {w.name} "
+                      f"({fl:.3g} FLOP in {dt:.1f} s, f64, {cores} threads)"}
+
+
+# ------------------------------------------------------------------- our arm
+
+def run_ours(args, rank: int, world: int, dist_on: bool):
+    import split_kv_attention_flash_gb300 as skv
+    from split_kv_attention_flash_gb300 import _build
+    if rank == 0 or not dist_on:
+        _build.build()
+    if dist_on:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = wl.ALL[args.workload]
+    if args.split is not None:
+        w = w.with_(split_kv=args.split)
+    q, k, v = w.make_inputs(dev)
+    p = skv.params_for(w, dev)
+    S = skv.sk_auto_split_kv(p)
+    p.split_kv = S
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=q.dtype, device=dev)
+    lse = None
+    ws = torch.empty(max(skv.sk_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+    kname = skv.sk_partial_kernel_name(p, q, k, v)
+    fl = flops_of(w)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        skv.sk_attn_fwd(p, q, k, v, out, lse, ws)
+
+    launches_per_step = 1 if S == 1 else 3
+    sampler = ClockSampler(dev.index)
+    with sampler:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if dist_on:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist_on:
+            torch.distributed.barrier()
+        ms = e0.elapsed_time(e1) / args.steps
+
+        # the partial kernel alone (dominant kernel), same stream
+        o_part = torch.empty(w.H, S, w.total_q, w.d_v, dtype=torch.float32, device=dev)
+        l_part = torch.empty(w.H, S, w.total_q, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            skv.sk_attn_partial_fwd(p, q, k, v, o_part, l_part)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        n_part = max(args.steps, 5)
+        for _ in range(n_part):
+            skv.sk_attn_partial_fwd(p, q, k, v, o_part, l_part)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        part_ms = e0.elapsed_time(e1) / n_part
+
+        # the combine alone, L2 flushed before each launch
+        counts = torch.empty(w.total_q, dtype=torch.int32, device=dev)
+        skv.sk_valid_split_counts(p, counts)
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        comb_ms = []
+        for i in range(max(args.steps // 4, 10) + 3):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            skv.sk_combine(p, o_part, l_part, counts, out, None)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                comb_ms.append(a.elapsed_time(b))
+        comb_ms = statistics.median(comb_ms)
+        del flush
+
+        # end to end through the public call: pinned host inputs in, output back
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            skv.sk_attn_fwd(p, dq, dk, dv, out, None, ws)
+            hout.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(args.steps // 4, 5)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+    clocks = sampler.summary()
+
+    if dist_on:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    peaks = measured_peaks()
+    counts_np = counts.cpu().numpy()
+    cbytes = combine_bytes(w, counts_np, with_lse=False)
+    part_tflops = fl / (part_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(kname)
+    line = {
+        "metric": METRIC, "value": world * fl / (ms * 1e-3) / 1e12, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (world * fl / (ms * 1e-3) / 1e12) / PAGES_SPLIT3_TFLOPS,
+        "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "sequences": w.B, "seq_len_q": list(w.seqlens_q),
+                   "seq_len_k": list(w.seqlens_k), "heads": w.H, "d_qk": w.d_qk, "d_v": w.d_v,
+                   "split_kv": S, "n_per_block": w.n_per_block,
+                   "block_m": skv.sk_default_block_m(w.d_qk, w.d_v),
+                   "flop_per_step": fl, "l2": "inputs larger than L2 "
+                   f"({(q.numel() + k.numel() + v.numel()) * q.element_size() / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": kname, "bound": "tensor", "achieved": part_tflops,
+                     "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": part_tflops / peaks["bf16"],
+                     "peak_source": f"{peaks['source']} dense bf16 burst",
+                     "ms_per_launch": part_ms,
+                     "traffic": traffic},
+        "combine": {"achieved": cbytes / (comb_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "peak": peaks["hbm"], "frac": cbytes / (comb_ms * 1e-3) / 1e9 / peaks["hbm"],
+                    "bytes": cbytes, "us_per_launch": comb_ms * 1e3, "l2": "flushed"},
+        "e2e": {"value": world * fl / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * q.element_size()),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(w, args.cpu_seconds)
+    return line
+
+
+def run_reference(args, rank: int):
+    """The reference arm: the CPU oracle as it stands, on host cores, rank 0 only."""
+    if rank != 0:
+        return None
+    w = wl.ALL[args.workload]
+    import oracle
+    oracle.build()
+    per_step = max(args.cpu_seconds / max(args.steps + args.warmup, 1), 0.5)
+    inputs = w.make_inputs("cpu")
+    vals = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        r = time_oracle(w, per_step, seed=i, inputs=inputs)
+        if i >= args.warmup:
+            vals.append(r["value"])
+            base = r
+    value = statistics.mean(vals)
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": value / PAGES_SPLIT3_TFLOPS, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "heads": w.H, "d_qk": w.d_qk, "d_v": w.d_v},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": base["cores"],
+                             "kind": "oracle", "sample": base["sample"] + " per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(wl.ALL), default="target")
+    ap.add_argument("--split", type=int, default=None, help="force split_kv (default: auto)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist_on = world > 1
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if dist_on:
+        torch.distributed.init_process_group("nccl")
+    try:
+        line = run_ours(args, rank, world, dist_on)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if dist_on:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

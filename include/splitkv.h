@@ -1,0 +1,193 @@
+/*
+ * splitkv.h -- C ABI of a split-KV attention forward pass for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   [P1] "Recombine fully masked split-KV attention partials on the host"
+ *        (ROCm/rocmlirTriton pull request 535)
+ *   [P2] "[ASM] [HIP] [JIT] [gfx942] Optimize long-context FMHA with split-KV"
+ *        (ROCm/aiter pull request 5592)
+ *   [P3] "[HIP] MHA v4: check Q scale backing only on the sparse path"
+ *        (ROCm/aiter pull request 7651) -- only its convention that an
+ *        incompatible input gets a clear error rather than a fault.
+ *
+ * The method ([P1] Summary): each (batch-head, M block of queries) splits its keys
+ * into split_kv chunks; one partial output O_s and one log-sum-exp L_s are written
+ * per split (an empty split writes O_s = 0 and L_s = -inf); a combine stage merges
+ * the partials with per-row valid-split counts, NaN-safely and in f32.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     never allocates, frees or synchronises (except sk_read_device_error, which
+ *     says so). Every compute call only enqueues work on `stream` and returns.
+ *   - Validation happens on the host before any launch. A rejected call returns
+ *     SK_ERR_INVALID_ARG or SK_ERR_UNSUPPORTED and launches nothing ([P2] Technical
+ *     details: incompatible requests raise; [P3] Summary: a clear error, not a fault).
+ *     A launch failure returns SK_ERR_CUDA.
+ *   - Device data (cu_seqlens) cannot be checked on the host without a sync. The
+ *     kernels clamp every sequence to max_seqlen_{q,k} and to total_{q,k}, so bad
+ *     cu_seqlens give wrong numbers but never an out-of-bounds access.
+ *   - Packed row r of sequence b (varlen) is query/key position r - cu_seqlens[b].
+ *     Without cu_seqlens (dense layout) sequence b has max_seqlen_{q,k} rows and
+ *     packed row index b * max_seqlen + position.
+ *   - Partial buffers: o_part f32 [H][S][total_q][d_v], lse_part f32 [H][S][total_q]
+ *     (the split axis sits next to the batch-head axis, as in [P1] per-row mask
+ *     layout). Final LSE: f32 [H][total_q]. Counts: int32 [total_q] (one count per
+ *     packed row, the same for every head -- [P1] layout [batchHeads, 1, seq_len_q, 1]
+ *     broadcast over heads).
+ *   - Log-sum-exps are natural logs of the scaled scores softmax_scale * q.k.
+ */
+#ifndef SPLITKV_H
+#define SPLITKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *sk_stream;
+
+typedef enum {
+    SK_OK = 0,
+    SK_ERR_INVALID_ARG = 1,   /* a null pointer, a negative size, inconsistent fields */
+    SK_ERR_UNSUPPORTED = 2,   /* valid but not implemented: head dims, dtype mix, alignment */
+    SK_ERR_WORKSPACE = 3,     /* workspace_bytes smaller than sk_workspace_bytes() */
+    SK_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
+    SK_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (sk_read_device_error) */
+} sk_status;
+
+typedef enum { SK_BF16 = 0, SK_F16 = 1, SK_F32 = 2 } sk_dtype;
+
+/* [P1] Technical details: under causal and prefix-causal masking key j is visible to
+ * query q when j <= q + prefix_offset (prefix_offset is 0 for plain causal);
+ * under every mask j must also be <= lastValid. */
+typedef enum { SK_MASK_NONE = 0, SK_MASK_CAUSAL = 1, SK_MASK_PREFIX_CAUSAL = 2 } sk_mask;
+
+/* A [rows, heads, dim] (varlen) or [batch, rows, heads, dim] (dense) tensor with a
+ * contiguous innermost dimension. Strides are in elements. The base pointer and
+ * every stride times the element size must be multiples of 16 bytes. */
+typedef struct {
+    void *ptr;
+    sk_dtype dtype;
+    int64_t stride_b;     /* between sequences; dense layout only (ignored with cu_seqlens) */
+    int64_t stride_row;   /* between consecutive rows (tokens) */
+    int64_t stride_h;     /* between heads */
+} sk_tensor;
+
+typedef struct {
+    int B;                       /* number of sequences (>= 1) */
+    int H;                       /* heads (>= 1); K and V have H heads too */
+    int max_seqlen_q;            /* >= every query length */
+    int max_seqlen_k;            /* >= every key length; 0 is allowed ([P2] empty-K review) */
+    int total_q;                 /* packed query rows (dense: B * max_seqlen_q) */
+    int total_k;                 /* packed key rows (dense: B * max_seqlen_k) */
+    int d_qk;                    /* head dim of Q and K ([P2] Motivation: 192) */
+    int d_v;                     /* head dim of V and of the output ([P2]: 128) */
+    const int32_t *cu_seqlens_q; /* device int32 [B+1], or NULL together with cu_seqlens_k */
+    const int32_t *cu_seqlens_k; /* device int32 [B+1], or NULL (dense layout) */
+    sk_mask mask;
+    int prefix_offset;           /* must be 0 unless mask == SK_MASK_PREFIX_CAUSAL */
+    int last_valid_kv_index;     /* -1: each sequence's last key; else min(this, Sk_b - 1) */
+    int n_per_block;             /* the key tile nPerBlock of the partition (>= 1) */
+    int split_kv;                /* 0: automatic (sk_auto_split_kv); else 1..32 */
+    int block_m;                 /* query rows per M block of the partition; 0: default */
+    float softmax_scale;         /* 0: 1/sqrt(d_qk) */
+} sk_params;
+
+/* Head-dimension pairs (d_qk, d_v) the kernels are built for. */
+#define SK_MAX_SPLIT_KV 32
+
+/*
+ * sk_valid_split_counts -- [P1] Technical details, per-row valid-split counts
+ * (computeValidSplitKV). For packed query row r at position q of sequence b:
+ *   rowLast      = clamp(q + prefix_offset, 0, lastValid)   (causal / prefix-causal)
+ *                = lastValid                                 (no mask)
+ *   keysPerSplit = n_per_block * ceil(ceil((rowLast + 1) / n_per_block) / S)
+ *   counts[r]    = ceil((rowLast + 1) / keysPerSplit)
+ * A sequence without keys gets count 1. S is split_kv after resolving 0 (auto).
+ * counts: device int32 [total_q]. Exact integer arithmetic.
+ */
+sk_status sk_valid_split_counts(const sk_params *p, int32_t *counts, sk_stream stream);
+
+/*
+ * sk_attn_partial_fwd -- [P1] Summary and Technical details; [P2] Technical details.
+ * For every (sequence, head, M block of block_m query rows, split s) the block's keys
+ * 0..blockLast (blockLast = rowLast of the block's last row) are cut into key tiles of
+ * n_per_block and dealt out in runs of itersPerBlock = ceil(tiles / S); split s gets
+ * run s. Over the keys of its run that row q may see:
+ *   O_s = sum_j softmax(scale * q.k_j) v_j        L_s = log sum_j exp(scale * q.k_j)
+ * A row with no visible key in the split gets O_s = 0 and L_s = -inf ([P1]: the
+ * kernel writes zero output and -inf LSE for empty splits).
+ * q, k, v: storage bf16 / f16 / f32, all the same dtype.
+ * o_part: device f32 [H][S][total_q][d_v]; lse_part: device f32 [H][S][total_q].
+ */
+sk_status sk_attn_partial_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
+                              float *o_part, float *lse_part, sk_stream stream);
+
+/*
+ * sk_combine -- [P1] Technical details, NaN-safe merge (computeFinalAttentionStage)
+ * and f32 merge for f16/bf16. Per (head, row), over the splits s < counts[row] only
+ * (the others are never read):
+ *   m = max(max_s L_s, lowest finite f32);  w_s = exp(L_s - m)
+ *   O = sum_s w_s O_s / max(sum_s w_s, 1)   (in f32, then cast to out.dtype)
+ *   lse_out = m + log(sum_s w_s), or -inf when that sum is 0
+ * out: [rows, H, d_v] or dense, dtype = storage type; lse_out may be NULL ([P2]
+ * review: return_lse=False passes a null LSE to the combine).
+ */
+sk_status sk_combine(const sk_params *p, const float *o_part, const float *lse_part,
+                     const int32_t *counts, sk_tensor out, float *lse_out, sk_stream stream);
+
+/*
+ * sk_attn_fwd -- the whole forward pass in one call: counts, partials, combine.
+ * With S == 1 the partial kernel writes `out` and `lse_out` directly and no
+ * workspace is used. Otherwise `workspace` (device, 256-byte aligned, at least
+ * sk_workspace_bytes()) holds the counts and the partials. max_seqlen_k == 0 writes
+ * O = 0 and LSE = -inf ([P2] review: forced split with empty K must not raise;
+ * [P1]: an empty split's LSE is -inf). lse_out may be NULL.
+ */
+sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v, sk_tensor out,
+                      float *lse_out, void *workspace, size_t workspace_bytes, sk_stream stream);
+
+/* Bytes of workspace sk_attn_fwd needs for these parameters (0 when S == 1).
+ * Resolving split_kv = 0 reads the current device's SM count. */
+sk_status sk_workspace_bytes(const sk_params *p, size_t *bytes);
+
+/*
+ * sk_auto_split_kv -- [P2] Technical details: num_splits 0 is auto, 1 keeps the
+ * unsplit kernel, 2..8 (here 2..32) force that split. Auto uses 3 splits when
+ * max_seqlen_k >= 8192 (an explicit boundary, as the review asks) and
+ * ceil(max_seqlen_q / block_m) * H <= 2 * SM count; otherwise 1. For single-query
+ * problems (max_seqlen_q == 1) it takes the smallest S <= 32 with B * H * S >= 2 * SM
+ * count. A non-zero split_kv is returned unchanged. Reads the current device.
+ */
+sk_status sk_auto_split_kv(const sk_params *p, int *split_kv_out);
+
+/* Host-only form of sk_auto_split_kv with the SM count given. */
+sk_status sk_choose_split_kv(const sk_params *p, int sm_count, int *split_kv_out);
+
+/* The M block (block_m = 0) the library uses for these head dims and dtype: 256. */
+int sk_default_block_m(int d_qk, int d_v, sk_dtype dtype);
+
+/* Whether (d_qk, d_v) is one of the supported head-dimension pairs. */
+int sk_supported_head_dims(int d_qk, int d_v);
+
+/* Name of the kernel sk_attn_partial_fwd would launch for these parameters, for
+ * logging and benchmarks; NULL when the call would be rejected. */
+const char *sk_partial_kernel_name(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v);
+
+/* Human-readable text of a status code. */
+const char *sk_status_string(sk_status s);
+
+/* Debug: reads (and optionally clears) the device error word that bounded waits
+ * set when they give up. SYNCHRONISES the current device. *code = 0: no error. */
+sk_status sk_read_device_error(int *code, int clear);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int sk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPLITKV_H */

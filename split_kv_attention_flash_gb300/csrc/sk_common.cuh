@@ -1,0 +1,173 @@
+// sk_common.cuh -- problem description and index arithmetic shared by the kernels.
+//
+// Page tags used in comments across csrc/:
+//   [P1] "Recombine fully masked split-KV attention partials on the host"
+//   [P2] "[ASM] [HIP] [JIT] [gfx942] Optimize long-context FMHA with split-KV"
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sk {
+
+// Storage types (same numbering as sk_dtype in include/splitkv.h).
+enum : int { kBF16 = 0, kF16 = 1, kF32 = 2 };
+
+// The validated problem, passed to every kernel by value.
+struct Problem {
+    int B, H, max_sq, max_sk, total_q, total_k, d_qk, d_v;
+    const int32_t *cu_q, *cu_k;  // device; both null for the dense layout
+    int causal;                  // 1 under causal or prefix-causal masking
+    int prefix_offset;           // 0 for plain causal
+    int last_valid_kv_index;     // -1: each sequence's last key
+    int bn;                      // key tile n_per_block
+    int S;                       // resolved split count
+    int bm;                      // M block rows of the partition
+    float scale;                 // softmax scale
+    float scale_log2;            // scale * log2(e): scores are kept in base 2
+    int *err;                    // device error word (bounded waits), may be null
+};
+
+// A [rows, heads, dim] view with element strides (dense layout adds stride_b).
+struct TensorView {
+    char *ptr;
+    int64_t sb, sr, sh;  // element strides
+};
+
+// Where sequence b lives, clamped so that bad cu_seqlens cannot index outside
+// [0, total) nor past max_seqlen.
+struct SeqInfo {
+    int q0, sq;        // first packed query row, query count
+    int k0, sk;        // first packed key row, key count
+    int last_valid;    // last key any query may see; -1 when there is none
+};
+
+__host__ __device__ inline int clamp_len(long long start, long long len, long long max_len,
+                                         long long total) {
+    if (len > max_len) len = max_len;
+    if (start < 0 || start >= total) return 0;
+    if (start + len > total) len = total - start;
+    return len < 0 ? 0 : (int)len;
+}
+
+__device__ inline SeqInfo seq_info(const Problem &p, int b) {
+    SeqInfo s;
+    long long q0, q1, k0, k1;
+    if (p.cu_q) {
+        q0 = __ldg(p.cu_q + b); q1 = __ldg(p.cu_q + b + 1);
+        k0 = __ldg(p.cu_k + b); k1 = __ldg(p.cu_k + b + 1);
+    } else {
+        q0 = (long long)b * p.max_sq; q1 = q0 + p.max_sq;
+        k0 = (long long)b * p.max_sk; k1 = k0 + p.max_sk;
+    }
+    s.q0 = (int)q0;
+    s.k0 = (int)k0;
+    s.sq = clamp_len(q0, q1 - q0, p.max_sq, p.total_q);
+    s.sk = clamp_len(k0, k1 - k0, p.max_sk, p.total_k);
+    int last = s.sk - 1;
+    if (p.last_valid_kv_index >= 0 && p.last_valid_kv_index < last) last = p.last_valid_kv_index;
+    s.last_valid = last;
+    return s;
+}
+
+// Element offset of row `pos` of sequence b in a tensor view.
+__device__ inline int64_t row_offset(const Problem &p, const TensorView &t, int b, int start,
+                                     int pos) {
+    return p.cu_q ? (int64_t)(start + pos) * t.sr : (int64_t)b * t.sb + (int64_t)pos * t.sr;
+}
+
+// Last key the partition must cover for `row` ([P1] Technical details):
+// clamp(row + prefix_offset, 0, lastValid) under causal masks, lastValid otherwise;
+// -1 when the sequence has no key.
+__host__ __device__ inline long long covered_last(const Problem &p, int last_valid, long long row) {
+    if (last_valid < 0) return -1;
+    if (!p.causal) return last_valid;
+    long long x = row + p.prefix_offset;
+    if (x < 0) x = 0;
+    if (x > last_valid) x = last_valid;
+    return x;
+}
+
+// [P1] per-row valid-split count (computeValidSplitKV).
+__host__ __device__ inline int valid_split_count(const Problem &p, int last_valid, int pos) {
+    long long rl = covered_last(p, last_valid, pos);
+    if (rl < 0) return 1;
+    long long n = rl + 1;
+    long long tiles = (n + p.bn - 1) / p.bn;
+    long long kps = (long long)p.bn * ((tiles + p.S - 1) / p.S);
+    return (int)((n + kps - 1) / kps);
+}
+
+// Keys [kb, ke) of split s for the M block that holds query `pos` ([P1]: the kernel
+// partitions each M block's keys by the block's last row, in runs of
+// itersPerBlock = ceil(tiles / S) key tiles).
+__host__ __device__ inline void split_key_range(const Problem &p, int sq, int last_valid, int pos,
+                                                int s, int &kb, int &ke) {
+    long long first = (long long)(pos / p.bm) * p.bm;
+    long long last_row = first + p.bm - 1;
+    if (last_row > sq - 1) last_row = sq - 1;
+    long long bl = covered_last(p, last_valid, last_row);
+    kb = ke = 0;
+    if (bl < 0) return;
+    long long nt = (bl + p.bn) / p.bn;
+    long long it = (nt + p.S - 1) / p.S;
+    long long t0 = (long long)s * it, t1 = t0 + it;
+    if (t1 > nt) t1 = nt;
+    if (t0 >= t1) return;
+    kb = (int)(t0 * p.bn);
+    long long e = t1 * p.bn;
+    ke = (int)(e < bl + 1 ? e : bl + 1);
+}
+
+// Last key query `pos` may see, ignoring the split: lastValid, and q + offset
+// under a causal mask. Negative when the row sees nothing.
+__device__ inline long long row_limit(const Problem &p, int last_valid, int pos) {
+    long long lim = last_valid;
+    if (p.causal) {
+        long long c = (long long)pos + p.prefix_offset;
+        if (c < lim) lim = c;
+    }
+    return lim;
+}
+
+// ---------------------------------------------------------------- conversions
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) {
+    return __float2half_rn(x);
+}
+
+// Warp reductions over groups of W consecutive lanes (W a power of two <= 32).
+template <int W> __device__ __forceinline__ float group_max(float x) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+template <int W> __device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace sk
+
+// Launchers implemented in the .cu files (host side).
+namespace sk {
+cudaError_t launch_counts(const Problem &p, int32_t *counts, cudaStream_t st);
+cudaError_t launch_partial_simt(const Problem &p, int dtype, const TensorView &q,
+                                const TensorView &k, const TensorView &v, float *o_part,
+                                float *lse_part, const TensorView *out, float *lse_out,
+                                cudaStream_t st);
+cudaError_t launch_combine(const Problem &p, int dtype, const float *o_part,
+                           const float *lse_part, const int32_t *counts, const TensorView &out,
+                           float *lse_out, cudaStream_t st);
+}  // namespace sk

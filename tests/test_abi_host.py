@@ -1,0 +1,153 @@
+"""Host-side checks of the C ABI (no GPU): every declared symbol is exported,
+argument validation returns the documented statuses before any launch, the
+automatic split choice follows the pages' rule, and workspace sizes add up."""
+from __future__ import annotations
+
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import split_kv_attention_flash_gb300 as skv
+from split_kv_attention_flash_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "splitkv.h")
+FAKE = 0x7f0000001000          # a 4 KiB-aligned address that is never dereferenced
+
+SK_OK, SK_ERR_INVALID_ARG, SK_ERR_UNSUPPORTED, SK_ERR_WORKSPACE = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return skv.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sk_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary_calls():
+    names = _declared_functions()
+    for n in ("sk_valid_split_counts", "sk_attn_partial_fwd", "sk_combine", "sk_attn_fwd",
+              "sk_workspace_bytes", "sk_auto_split_kv"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in _declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def _params(**kw):
+    base = dict(B=2, H=4, max_seqlen_q=64, max_seqlen_k=512, total_q=100, total_k=700, d_qk=128,
+                d_v=128, cu_seqlens_q=FAKE, cu_seqlens_k=FAKE + 256, n_per_block=64, split_kv=3)
+    base.update(kw)
+    return skv.Params(**base)
+
+
+def _t(dtype=skv.SK_BF16, ptr=FAKE, sb=0, sr=512, sh=128):
+    return skv._Tensor(ptr, dtype, sb, sr, sh)
+
+
+def _fwd(L, p, q=None, k=None, v=None, out=None, ws=FAKE, ws_bytes=1 << 40):
+    q, k, v, out = q or _t(), k or _t(), v or _t(), out or _t()
+    return L.sk_attn_fwd(ctypes.byref(p.c()), q, k, v, out, None, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), SK_ERR_INVALID_ARG),
+    (dict(H=0), SK_ERR_INVALID_ARG),
+    (dict(total_q=-1), SK_ERR_INVALID_ARG),
+    (dict(cu_seqlens_k=None), SK_ERR_INVALID_ARG),
+    (dict(cu_seqlens_q=None, cu_seqlens_k=None), SK_ERR_INVALID_ARG),  # dense totals mismatch
+    (dict(prefix_offset=3), SK_ERR_INVALID_ARG),
+    (dict(mask=skv.MASK_CAUSAL, prefix_offset=3), SK_ERR_INVALID_ARG),
+    (dict(mask=7), SK_ERR_INVALID_ARG),
+    (dict(last_valid_kv_index=-2), SK_ERR_INVALID_ARG),
+    (dict(n_per_block=0), SK_ERR_INVALID_ARG),
+    (dict(split_kv=33), SK_ERR_INVALID_ARG),
+    (dict(split_kv=-1), SK_ERR_INVALID_ARG),
+    (dict(block_m=-4), SK_ERR_INVALID_ARG),
+    (dict(softmax_scale=float("nan")), SK_ERR_INVALID_ARG),
+    (dict(d_qk=96, d_v=96), SK_ERR_UNSUPPORTED),
+    (dict(d_qk=128, d_v=64), SK_ERR_UNSUPPORTED),
+])
+def test_invalid_params_rejected_before_launch(L, kw, status):
+    assert _fwd(L, _params(**kw)) == status
+
+
+def test_invalid_tensors_rejected_before_launch(L):
+    p = _params()
+    assert _fwd(L, p, q=_t(ptr=0)) == SK_ERR_INVALID_ARG                   # null
+    assert _fwd(L, p, q=_t(ptr=FAKE + 8)) == SK_ERR_UNSUPPORTED            # 8-byte aligned only
+    assert _fwd(L, p, k=_t(sr=500 + 3)) == SK_ERR_UNSUPPORTED              # 1006-byte row stride
+    assert _fwd(L, p, v=_t(dtype=skv.SK_F16)) == SK_ERR_UNSUPPORTED        # mixed storage types
+    assert _fwd(L, p, out=_t(dtype=skv.SK_F32)) == SK_ERR_UNSUPPORTED      # output not storage type
+    assert _fwd(L, p, q=_t(dtype=9)) == SK_ERR_INVALID_ARG
+    assert _fwd(L, p, q=_t(sr=-512)) == SK_ERR_INVALID_ARG
+
+
+def test_workspace_too_small(L):
+    p = _params(split_kv=3)
+    need = skv.sk_workspace_bytes(p)
+    assert need > 0
+    assert _fwd(L, p, ws_bytes=need - 1) == SK_ERR_WORKSPACE
+    assert _fwd(L, p, ws=FAKE + 16, ws_bytes=need) == SK_ERR_INVALID_ARG  # not 256-byte aligned
+
+
+def test_workspace_layout_sizes(L):
+    def a256(x):
+        return (x + 255) // 256 * 256
+    for S, tq, H, dv in ((3, 100, 4, 128), (8, 16384, 12, 128), (2, 1, 1, 64)):
+        p = _params(split_kv=S, total_q=tq, H=H, d_qk=dv, d_v=dv)
+        assert skv.sk_workspace_bytes(p) == a256(4 * tq) + a256(4 * H * S * tq * dv) + a256(4 * H * S * tq)
+    assert skv.sk_workspace_bytes(_params(split_kv=1)) == 0
+
+
+def test_partial_and_combine_validation(L):
+    p = _params()
+    c = ctypes.byref(p.c())
+    assert L.sk_attn_partial_fwd(c, _t(), _t(), _t(), None, FAKE, None) == SK_ERR_INVALID_ARG
+    assert L.sk_attn_partial_fwd(c, _t(), _t(), _t(), FAKE + 4, FAKE, None) == SK_ERR_UNSUPPORTED
+    assert L.sk_combine(c, FAKE, FAKE, None, _t(), None, None) == SK_ERR_INVALID_ARG
+    assert L.sk_valid_split_counts(c, None, None) == SK_ERR_INVALID_ARG
+    assert L.sk_valid_split_counts(None, FAKE, None) == SK_ERR_INVALID_ARG
+
+
+def test_auto_split_boundary_from_the_pages(L):
+    data = json.load(open(os.path.join(ROOT, "tests", "golden", "auto_split_boundary.json")))
+    for c in data["cases"]:
+        p = _params(B=1, H=c["H"], max_seqlen_q=c["max_seqlen_q"], max_seqlen_k=c["max_seqlen_k"],
+                    total_q=c["max_seqlen_q"], total_k=c["max_seqlen_k"], split_kv=0,
+                    block_m=data["block_m"])
+        assert skv.sk_choose_split_kv(p, data["sm_count"]) == c["split_kv"], c
+
+
+def test_auto_split_rules(L):
+    # forced values pass through
+    for s in range(1, 33):
+        assert skv.sk_choose_split_kv(_params(split_kv=s), 152) == s
+    # single-query problems: smallest S with B*H*S >= 2*SM
+    dec = dict(max_seqlen_q=1, max_seqlen_k=100000, total_q=32, total_k=3200000, split_kv=0)
+    assert skv.sk_choose_split_kv(_params(B=32, H=32, **dec), 152) == 1
+    assert skv.sk_choose_split_kv(_params(B=4, H=8, **dec), 152) == 10
+    assert skv.sk_choose_split_kv(_params(B=1, H=8, **dec), 152) == 32
+    # the default M block enters Q_tiles
+    p = _params(B=1, H=12, max_seqlen_q=4096, max_seqlen_k=42700, total_q=4096, total_k=42700,
+                split_kv=0)
+    assert skv.sk_default_block_m(192, 128) == 256
+    assert skv.sk_choose_split_kv(p, 152) == 3
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert skv.sk_status_string(code)
+    assert "unknown" in skv.sk_status_string(99)
+    assert L.sk_version() >= 100
+    assert L.sk_supported_head_dims(192, 128) and not L.sk_supported_head_dims(192, 192)

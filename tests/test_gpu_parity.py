@@ -1,0 +1,274 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Small problems (several M blocks and key tiles, ragged tails, every mask, every
+storage type and head-dim pair) are compared element by element; the full-size
+workloads are compared on sampled rows (all heads; per sequence the first and
+last rows plus seeded random rows). Split counts are compared bit-exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import split_kv_attention_flash_gb300 as skv
+from split_kv_attention_flash_gb300 import workloads as wl
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from split_kv_attention_flash_gb300 import _build
+    _build.build()
+    skv.lib()
+
+
+def _small(dtype, dqk, dv, mask=wl.MASK_NONE, po=0, lvi=-1, bn=64, S=3, seed=0,
+           sq=(300, 1, 77, 256), sk=(1000, 5, 0, 513)):
+    return wl.Workload(f"small {dtype} {dqk}/{dv} mask{mask} po{po} lvi{lvi} S{S}", H=2,
+                       seqlens_q=sq, seqlens_k=sk, d_qk=dqk, d_v=dv, dtype=dtype, seed=seed,
+                       n_per_block=bn, split_kv=S, mask=mask, prefix_offset=po,
+                       last_valid_kv_index=lvi)
+
+
+SMALL = [
+    wl.TINY_CAUSAL,
+    _small("bf16", 128, 128),
+    _small("bf16", 192, 128, mask=wl.MASK_CAUSAL, S=4, bn=128),
+    _small("f16", 64, 64, mask=wl.MASK_PREFIX_CAUSAL, po=40, lvi=700, S=5, bn=32),
+    _small("f16", 128, 128, mask=wl.MASK_PREFIX_CAUSAL, po=-100, S=2, bn=16),
+    _small("f32", 192, 128, mask=wl.MASK_CAUSAL, lvi=200, S=8, bn=48),
+    _small("bf16", 64, 64, S=1),
+    _small("bf16", 192, 128, S=7, bn=128, sq=(1, 1, 1), sk=(3000, 17, 0)),
+]
+
+
+def _inputs(w):
+    q, k, v = w.make_inputs("cpu")
+    return (q, k, v), (q.to(DEV), k.to(DEV), v.to(DEV))
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_counts_bit_exact_small(w):
+    S = H.resolved_split(w, DEV)
+    p = skv.params_for(w, DEV, split_kv=S)
+    counts = torch.full((w.total_q,), -7, dtype=torch.int32, device=DEV)
+    skv.sk_valid_split_counts(p, counts)
+    ref = oracle.split_counts(H.oracle_problem(w, S))
+    assert np.array_equal(counts.cpu().numpy(), ref)
+
+
+def test_counts_bit_exact_sweep():
+    rng = np.random.default_rng(123)
+    for _ in range(150):
+        B = int(rng.integers(1, 4))
+        sq = tuple(int(x) for x in rng.integers(1, 70, B))
+        sk = tuple(int(x) for x in rng.integers(0, 300, B))
+        mask = int(rng.integers(0, 3))
+        po = int(rng.integers(-80, 300)) if mask == wl.MASK_PREFIX_CAUSAL else 0
+        w = wl.Workload("sweep", H=1, seqlens_q=sq, seqlens_k=sk, d_qk=64, d_v=64, dtype="bf16",
+                        seed=0, n_per_block=int(rng.choice([1, 16, 32, 48, 128])),
+                        split_kv=int(rng.integers(1, 33)), mask=mask, prefix_offset=po,
+                        last_valid_kv_index=int(rng.choice([-1, 0, 50, 1000])))
+        p = skv.params_for(w, DEV)
+        counts = torch.empty(w.total_q, dtype=torch.int32, device=DEV)
+        skv.sk_valid_split_counts(p, counts)
+        ref = oracle.split_counts(H.oracle_problem(w, w.split_kv))
+        assert np.array_equal(counts.cpu().numpy(), ref), w
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_partials_match_oracle_small(w):
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    S = H.resolved_split(w, DEV)
+    o_part, l_part, _ = H.run_partials(w, qd, kd, vd, DEV, S)
+    ref_o, ref_l = oracle.partials(H.oracle_problem(w, S), q, k, v)      # [n, H, S, dv]
+    got_o = o_part.permute(2, 0, 1, 3).cpu().numpy()
+    got_l = l_part.permute(2, 0, 1).cpu().numpy()
+    H.assert_close(got_o, got_l, ref_o, ref_l, w.dtype, "partials")
+    # empty (row, split) pairs: exact zero output and -inf LSE
+    empty = np.isneginf(ref_l)
+    assert (got_o[empty] == 0).all() and np.isneginf(got_l[empty]).all()
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_forward_matches_oracle_small(w):
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    out, lse, p = H.run_fwd(w, qd, kd, vd, DEV)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
+    # without an LSE output the output is identical
+    out2, _, _ = H.run_fwd(w, qd, kd, vd, DEV, with_lse=False)
+    assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("w", SMALL[:4], ids=lambda w: w.name)
+def test_split_one_direct_equals_partial_plus_combine(w):
+    (_, _, _), (qd, kd, vd) = _inputs(w)
+    out, lse, p = H.run_fwd(w, qd, kd, vd, DEV, split_kv=1)
+    o_part, l_part, p1 = H.run_partials(w, qd, kd, vd, DEV, 1)
+    counts = torch.empty(w.total_q, dtype=torch.int32, device=DEV)
+    skv.sk_valid_split_counts(p1, counts)
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    skv.sk_combine(p1, o_part, l_part, counts, out2, lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+    assert torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("w", SMALL[1:4], ids=lambda w: w.name)
+def test_combine_never_reads_invalid_splits(w):
+    (_, _, _), (qd, kd, vd) = _inputs(w)
+    S = H.resolved_split(w, DEV)
+    o_part, l_part, p = H.run_partials(w, qd, kd, vd, DEV, S)
+    counts = torch.empty(w.total_q, dtype=torch.int32, device=DEV)
+    skv.sk_valid_split_counts(p, counts)
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=qd.dtype, device=DEV)
+    lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=DEV)
+    skv.sk_combine(p, o_part, l_part, counts, out, lse)
+    s_idx = torch.arange(S, device=DEV)[None, :, None]
+    invalid = s_idx >= counts[None, None, :]                       # [1, S, total_q]
+    o_bad = o_part.masked_fill(invalid[..., None], float("nan"))
+    l_bad = l_part.masked_fill(invalid, float("nan"))
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    skv.sk_combine(p, o_bad, l_bad, counts, out2, lse2)
+    torch.cuda.synchronize()
+    assert invalid.any() or S == 1
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    assert not torch.isnan(out2.float()).any()
+
+
+def test_dense_layout_equals_varlen():
+    w = wl.Workload("dense", H=3, seqlens_q=(130, 130), seqlens_k=(400, 400), d_qk=128, d_v=128,
+                    dtype="bf16", seed=9, n_per_block=64, split_kv=3, mask=wl.MASK_CAUSAL)
+    (_, _, _), (qd, kd, vd) = _inputs(w)
+    out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
+    p = skv.params_for(w, DEV)
+    p.cu_seqlens_q = p.cu_seqlens_k = None
+    qb = qd.view(2, 130, 3, 128)
+    kb, vb = kd.view(2, 400, 3, 128), vd.view(2, 400, 3, 128)
+    outb = torch.empty(2, 130, 3, 128, dtype=qd.dtype, device=DEV)
+    lseb = torch.empty(3, 260, dtype=torch.float32, device=DEV)
+    ws = torch.empty(skv.sk_workspace_bytes(p), dtype=torch.uint8, device=DEV)
+    skv.sk_attn_fwd(p, qb, kb, vb, outb, lseb, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(outb.view_as(out), out) and torch.equal(lseb, lse)
+
+
+def test_strided_heads_and_rows():
+    """Q/K/V as views into wider buffers (row stride > H * d)."""
+    w = _small("bf16", 128, 128, mask=wl.MASK_CAUSAL, S=3)
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    pad = 8
+    def widen(t):
+        big = torch.zeros(t.shape[0], t.shape[1] + 1, t.shape[2] + pad, dtype=t.dtype, device=DEV)
+        big[:, 1:, pad:] = t
+        return big[:, 1:, pad:]
+    out_ref, lse_ref, p = H.run_fwd(w, qd, kd, vd, DEV)
+    qs, ks, vs = widen(qd), widen(kd), widen(vd)
+    out = widen(torch.empty_like(out_ref))
+    lse = torch.empty_like(lse_ref)
+    ws = torch.empty(skv.sk_workspace_bytes(p), dtype=torch.uint8, device=DEV)
+    skv.sk_attn_fwd(p, qs, ks, vs, out, lse, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
+
+
+def test_empty_keys_give_zero_and_neg_inf():
+    for S in (1, 4):
+        w = wl.Workload("no keys", H=2, seqlens_q=(5, 9), seqlens_k=(0, 0), d_qk=128, d_v=128,
+                        dtype="bf16", seed=1, n_per_block=128, split_kv=S)
+        (_, _, _), (qd, kd, vd) = _inputs(w)
+        kd = torch.zeros(1, 2, 128, dtype=qd.dtype, device=DEV)   # a real (unused) buffer
+        vd = torch.zeros(1, 2, 128, dtype=qd.dtype, device=DEV)
+        out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
+        assert (out == 0).all() and torch.isneginf(lse).all()
+
+
+def test_graph_capture_and_replay():
+    w = _small("bf16", 192, 128, mask=wl.MASK_CAUSAL, S=4, bn=128)
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    out_ref, lse_ref, p = H.run_fwd(w, qd, kd, vd, DEV)
+    out = torch.empty_like(out_ref)
+    lse = torch.empty_like(lse_ref)
+    ws = torch.empty(skv.sk_workspace_bytes(p), dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        skv.sk_attn_fwd(p, qd, kd, vd, out, lse, ws, stream=s)   # warm up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        skv.sk_attn_fwd(p, qd, kd, vd, out, lse, ws)
+    out.zero_()
+    lse.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref)
+    # new inputs in the same buffers are picked up by the replay
+    qd.mul_(0.5)
+    out_new, lse_new, _ = H.run_fwd(w, qd, kd, vd, DEV)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_new) and torch.equal(lse, lse_new)
+
+
+# ------------------------------------------------------------ full-size configs
+
+def _sampled_check(w, splits, rows_kw=None, seq_subset=None):
+    """Run the full-size workload for each split count and compare sampled rows.
+
+    With seq_subset, the oracle sees only those sequences (their Q/K/V rows copied
+    out), which keeps host memory small for the decode workload."""
+    q, k, v = w.make_inputs(DEV)
+    seqs = list(range(w.B)) if seq_subset is None else list(seq_subset)
+    sub = w.with_(seqlens_q=tuple(w.seqlens_q[b] for b in seqs),
+                  seqlens_k=tuple(w.seqlens_k[b] for b in seqs))
+    def gather(t, cu):
+        return torch.cat([t[cu[b]:cu[b + 1]] for b in seqs]).cpu()
+    qc, kc, vc = gather(q, w.cu_seqlens_q), gather(k, w.cu_seqlens_k), gather(v, w.cu_seqlens_k)
+    sub_rows = H.sample_rows(sub, **(rows_kw or {}))
+    # packed row of the subset -> packed row of the full problem
+    full_of_sub = np.concatenate([np.arange(w.cu_seqlens_q[b], w.cu_seqlens_q[b + 1])
+                                  for b in seqs]).astype(np.int64)
+    rows = full_of_sub[sub_rows]
+    ref_o, ref_l = oracle.attention(H.oracle_problem(sub, 1), qc, kc, vc, rows=sub_rows)
+    del qc, kc, vc
+    for S in splits:
+        out, lse, p = H.run_fwd(w, q, k, v, DEV, split_kv=S)
+        H.assert_close(H.to_np(out, rows), H.lse_np(lse, rows), ref_o, ref_l, w.dtype,
+                       f"{w.name} S={S}")
+        S_res = skv.sk_auto_split_kv(p)
+        counts = torch.empty(w.total_q, dtype=torch.int32, device=DEV)
+        skv.sk_valid_split_counts(p, counts)
+        ref_c = oracle.split_counts(H.oracle_problem(w, S_res))
+        assert np.array_equal(counts.cpu().numpy(), ref_c)
+        del out, lse
+
+
+def test_config_noncausal_bf16_full():
+    _sampled_check(wl.NONCAUSAL_BF16, [1, 2, 4, 8])
+
+
+@pytest.mark.parametrize("mask,po", [(wl.MASK_CAUSAL, 0), (wl.MASK_PREFIX_CAUSAL, 2048),
+                                     (wl.MASK_PREFIX_CAUSAL, -256)])
+def test_config_masked_f16_full(mask, po):
+    _sampled_check(wl.MASKED_F16.with_(mask=mask, prefix_offset=po), [4])
+
+
+def test_config_long_varlen_full():
+    w = wl.LONG_VARLEN
+    assert H.resolved_split(w, DEV) == 3
+    _sampled_check(w, [0, 2, 3, 4, 5, 6, 7, 8], rows_kw=dict(head=16, tail=16, rand=16))
+
+
+def test_config_decode_full():
+    w = wl.DECODE
+    _sampled_check(w, [0, 1, 2, 4, 8, 16, 32], seq_subset=[0, 7, 19, 31])
