@@ -3,15 +3,33 @@
 
 namespace sk {
 
+// Tensor cores (tcgen05) for 16-bit storage with the library's M block and more
+// than 16 queries in the longest sequence; the streaming decode kernel for 16-bit
+// storage with at most 16 queries per sequence; the CUDA-core kernel for the rest
+// (f32 storage, other M blocks, no keys, tensors TMA cannot describe).
 const char *partial_kernel_name(const Problem &p, int dtype, const TensorView &q,
                                 const TensorView &k, const TensorView &v) {
-    (void)p; (void)dtype; (void)q; (void)k; (void)v;
+    (void)q; (void)k; (void)v;
+    if (tc::partial_tc_supported(p, dtype)) return "partial_tc";
+    if (dec::partial_decode_supported(p, dtype)) return "partial_decode";
     return "partial_simt";
 }
 
 cudaError_t run_partial(const Problem &p, int dtype, const TensorView &q, const TensorView &k,
                         const TensorView &v, float *o_part, float *lse_part, const TensorView *out,
                         float *lse_out, cudaStream_t st) {
+    if (tc::partial_tc_supported(p, dtype)) {
+        bool launched = false;
+        cudaError_t e = tc::launch_partial_tc(p, dtype, q, k, v, o_part, lse_part, out, lse_out, st,
+                                              &launched);
+        if (launched || e != cudaSuccess) return e;
+    }
+    if (dec::partial_decode_supported(p, dtype)) {
+        bool launched = false;
+        cudaError_t e = dec::launch_partial_decode(p, dtype, q, k, v, o_part, lse_part, out, lse_out,
+                                                   st, &launched);
+        if (launched || e != cudaSuccess) return e;
+    }
     return launch_partial_simt(p, dtype, q, k, v, o_part, lse_part, out, lse_out, st);
 }
 

@@ -1,0 +1,512 @@
+// partial_tc.cu -- split partials on the tcgen05 tensor cores (bf16 / f16 storage).
+//
+// [P1] Summary / Technical details; [P2] Technical details (split kernel plus a
+// separate LSE combine). One CTA owns one (sequence, head, split, M block of 256
+// query rows) and computes, over the keys of the split's run,
+//   O_s = sum_j softmax(scale q.k_j) v_j,  L_s = log sum_j exp(scale q.k_j)
+// with the causal / last-valid masks applied per row; rows without a visible key
+// write O_s = 0 and L_s = -inf.
+//
+// Design (GB300, one CTA per SM):
+//   * The M block is two 128-row MMA tiles Q0, Q1, kept in shared memory for the
+//     whole CTA (TMA, 128-byte swizzle). Keys stream through in tiles of 128.
+//   * Warp 8 (one lane) is the TMA producer: Q once, then K(j) and V(j) into
+//     rings of shared-memory stages guarded by full / empty mbarriers.
+//   * Warp 9 (one lane) issues the tcgen05 MMAs: S_t = Q_t K(j)^T into TMEM
+//     (128 f32 columns per tile), then O_t += P_t V(j) with P_t read from TMEM and
+//     V(j) from shared memory (MN-major operand). The order
+//       S0(0) S1(0) | PV0(0) S0(1) | PV1(0) S1(1) | PV0(1) S0(2) | ...
+//     keeps the tensor core busy on one tile while the other tile's softmax runs.
+//   * Warps 0-3 (tile 0) and 4-7 (tile 1) run the online softmax, one query row
+//     per thread (TMEM lane = row): load the S row, mask, update the running max
+//     m and sum l, write P (16-bit) over the first half of the S columns. When the
+//     max grows by more than 2^8 the row's O accumulator in TMEM is rescaled first
+//     (TMEM columns 256.. / 384..). Scores are kept in base 2 (scale * log2 e).
+//   * TMEM: S0/P0 cols [0,128), S1/P1 [128,256), O0 [256,256+DV), O1 [384,384+DV).
+//   * Every mbarrier wait is bounded (1 s); a timeout records an error code in the
+//     library's device error word, raises a CTA-wide abort flag, drains in-flight
+//     TMA loads and MMAs, frees TMEM and returns.
+#include <float.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "sk_common.cuh"
+#include "sm100_ptx.cuh"
+#include "sk_dispatch.h"
+
+namespace sk {
+namespace tc {
+
+constexpr int kBM = 256;         // query rows per CTA
+constexpr int kTileM = 128;      // rows per MMA tile
+constexpr int kBN = 128;         // keys per MMA tile
+constexpr int kThreads = 320;    // 8 softmax warps + producer warp + MMA warp
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kChunkBytes = 128 * 128;  // one 64-column (128-byte) swizzled panel of 128 rows
+constexpr uint64_t kTimeoutNs = 1000000000ull;
+constexpr float kRescaleThreshold = 8.f;  // log2 units: rescale O only when m grows by > 2^8
+constexpr int kMinQueries = 17;           // fewer queries per sequence go to the CUDA-core kernel
+
+enum ErrCode : int { kErrProducer = 0x101, kErrMma = 0x102, kErrSoftmax = 0x103 };
+
+template <int DQK, int DV> struct Cfg {
+    static constexpr int kQBytes = kTileM * DQK * 2;
+    static constexpr int kKBytes = kBN * DQK * 2;
+    static constexpr int kVBytes = kBN * DV * 2;
+    static constexpr int kKStages = DQK == 192 ? 2 : (DQK == 128 ? 3 : 4);
+    static constexpr int kVStages = DQK == 192 ? 1 : (DQK == 128 ? 2 : 4);
+    // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O done x2, drain
+    static constexpr int kBarQ = 0;
+    static constexpr int kBarKF = 1;
+    static constexpr int kBarKE = kBarKF + kKStages;
+    static constexpr int kBarVF = kBarKE + kKStages;
+    static constexpr int kBarVE = kBarVF + kVStages;
+    static constexpr int kBarS = kBarVE + kVStages;
+    static constexpr int kBarP = kBarS + 2;
+    static constexpr int kBarO = kBarP + 2;
+    static constexpr int kBarDrain = kBarO + 2;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kTileBytes = 2 * kQBytes + kKStages * kKBytes + kVStages * kVBytes;
+    static constexpr int kSmemBytes = 1024 + kTileBytes + kNumBars * 8 + 16;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "head dims");
+};
+
+// Wait of a whole warp: every lane polls, the warp leaves together.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          int *err, int code) {
+    const int lane = threadIdx.x & 31;
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        bool ok = ptx::mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if ((i & 63u) == 63u) {
+            int give_up = 0;
+            if (lane == 0) {
+                if (t0 == 0) t0 = ptx::globaltimer();
+                if (*abort) give_up = 1;
+                else if (ptx::globaltimer() - t0 > kTimeoutNs) {
+                    *abort = 1;
+                    if (err) atomicCAS(err, 0, code);
+                    give_up = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+        }
+    }
+}
+
+template <typename T, int DQK, int DV, bool DIRECT>
+__global__ void __maxnreg__(200)
+    partial_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, Problem p, float *o_part,
+                      float *lse_part, TensorView out, float *lse_out) {
+    using C = Cfg<DQK, DV>;
+    constexpr bool kBF16 = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+
+    const int mb = blockIdx.x, h = blockIdx.y;
+    const int s = blockIdx.z % p.S, b = blockIdx.z / p.S;
+    const SeqInfo si = seq_info(p, b);
+    const int pos0 = mb * kBM;
+    if (pos0 >= si.sq) return;  // uniform: the M block lies past this sequence
+    int kb, ke;
+    split_key_range(p, si.sq, si.last_valid, pos0, s, kb, ke);
+    const int n_tiles = ke > kb ? (ke - kb + kBN - 1) / kBN : 0;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
+    const uint32_t sQ = (raw_u32 + 1023u) & ~1023u;
+    const uint32_t sK = sQ + 2 * C::kQBytes;
+    const uint32_t sV = sK + C::kKStages * C::kKBytes;
+    const uint32_t bar0 = sV + C::kVStages * C::kVBytes;
+    uint8_t *const gen_base = smem_raw + (sQ - raw_u32);
+    uint32_t *const tmem_holder = (uint32_t *)(gen_base + (bar0 - sQ) + C::kNumBars * 8);
+    volatile int *const abort_flag = (volatile int *)(tmem_holder + 1);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(C::kBarQ), 1);
+        for (int i = 0; i < C::kKStages; ++i) {
+            ptx::mbar_init(bar(C::kBarKF + i), 1);
+            ptx::mbar_init(bar(C::kBarKE + i), 1);
+        }
+        for (int i = 0; i < C::kVStages; ++i) {
+            ptx::mbar_init(bar(C::kBarVF + i), 1);
+            ptx::mbar_init(bar(C::kBarVE + i), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bar(C::kBarS + t), 1);
+            ptx::mbar_init(bar(C::kBarP + t), kTileM);
+            ptx::mbar_init(bar(C::kBarO + t), 1);
+        }
+        ptx::mbar_init(bar(C::kBarDrain), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_holder), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    const bool dense = p.cu_q == nullptr;
+    const int cb = dense ? b : 0;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n_tiles > 0) {
+            ptx::prefetch_tensormap(&tmQ);
+            ptx::prefetch_tensormap(&tmK);
+            ptx::prefetch_tensormap(&tmV);
+            const int qrow = dense ? pos0 : si.q0 + pos0;
+            const int krow = (dense ? 0 : si.k0) + kb;
+            ptx::mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kQBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int c = 0; c < DQK / 64; ++c)
+                    ptx::tma_load_4d(sQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar(C::kBarQ),
+                                     c * 64, qrow + t * kTileM, h, cb);
+            int issued_k = 0, issued_v = 0;
+            bool ok = true;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int ks = j % C::kKStages, vs = j % C::kVStages;
+                ok = ptx::mbar_wait_bounded(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1,
+                                            abort_flag, p.err, kErrProducer, kTimeoutNs);
+                if (!ok) break;
+                ptx::mbar_arrive_expect_tx(bar(C::kBarKF + ks), C::kKBytes);
+                for (int c = 0; c < DQK / 64; ++c)
+                    ptx::tma_load_4d(sK + ks * C::kKBytes + c * kChunkBytes, &tmK,
+                                     bar(C::kBarKF + ks), c * 64, krow + j * kBN, h, cb);
+                issued_k = j + 1;
+                ok = ptx::mbar_wait_bounded(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1,
+                                            abort_flag, p.err, kErrProducer, kTimeoutNs);
+                if (!ok) break;
+                ptx::mbar_arrive_expect_tx(bar(C::kBarVF + vs), C::kVBytes);
+                for (int c = 0; c < DV / 64; ++c)
+                    ptx::tma_load_4d(sV + vs * C::kVBytes + c * kChunkBytes, &tmV,
+                                     bar(C::kBarVF + vs), c * 64, krow + j * kBN, h, cb);
+                issued_v = j + 1;
+            }
+            if (!ok) {
+                // drain: every load already issued must land before the CTA exits
+                int quiet = 0;
+                volatile int *no_abort = (volatile int *)&quiet;
+                ptx::mbar_wait_bounded(bar(C::kBarQ), 0, no_abort, nullptr, 0, kTimeoutNs);
+                for (int i = 0; i < C::kKStages && i < issued_k; ++i) {
+                    const int last = i + ((issued_k - 1 - i) / C::kKStages) * C::kKStages;
+                    ptx::mbar_wait_bounded(bar(C::kBarKF + i), (last / C::kKStages) & 1, no_abort,
+                                           nullptr, 0, kTimeoutNs);
+                }
+                for (int i = 0; i < C::kVStages && i < issued_v; ++i) {
+                    const int last = i + ((issued_v - 1 - i) / C::kVStages) * C::kVStages;
+                    ptx::mbar_wait_bounded(bar(C::kBarVF + i), (last / C::kVStages) & 1, no_abort,
+                                           nullptr, 0, kTimeoutNs);
+                }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t kIdescQK = ptx::idesc_f16(kBF16, false, false, kTileM, kBN);
+            constexpr uint32_t kIdescPV = ptx::idesc_f16(kBF16, false, true, kTileM, DV);
+            const uint32_t tS[2] = {tmem, tmem + 128u};
+            const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
+            auto issue_qk = [&](int t, int j) {
+                const uint32_t kbase = sK + (j % C::kKStages) * C::kKBytes;
+                const uint32_t qbase = sQ + t * C::kQBytes;
+#pragma unroll
+                for (int kk = 0; kk < DQK / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    ptx::mma_ss(tS[t], ptx::smem_desc_sw128(qbase + off, 16, 1024),
+                                ptx::smem_desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0);
+                }
+                ptx::tc_commit(bar(C::kBarS + t));
+            };
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t vbase = sV + (j % C::kVStages) * C::kVBytes;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    ptx::mma_ts(tO[t], tS[t] + kk * 8, ptx::smem_desc_sw128(vbase + kk * 2048, kChunkBytes, 1024),
+                                kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            };
+            bool ok = ptx::mbar_wait_bounded(bar(C::kBarQ), 0, abort_flag, p.err, kErrMma, kTimeoutNs) &&
+                      ptx::mbar_wait_bounded(bar(C::kBarKF), 0, abort_flag, p.err, kErrMma, kTimeoutNs);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_qk(0, 0);
+                issue_qk(1, 0);
+                ptx::tc_commit(bar(C::kBarKE));
+            }
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int vs = j % C::kVStages;
+                const int kn = (j + 1) % C::kKStages;
+                ok = ptx::mbar_wait_bounded(bar(C::kBarVF + vs), (j / C::kVStages) & 1, abort_flag,
+                                            p.err, kErrMma, kTimeoutNs) &&
+                     ptx::mbar_wait_bounded(bar(C::kBarP + 0), j & 1, abort_flag, p.err, kErrMma,
+                                            kTimeoutNs);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                issue_pv(0, j);
+                if (j + 1 < n_tiles) {
+                    ok = ptx::mbar_wait_bounded(bar(C::kBarKF + kn), ((j + 1) / C::kKStages) & 1,
+                                                abort_flag, p.err, kErrMma, kTimeoutNs);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_qk(0, j + 1);
+                }
+                ok = ptx::mbar_wait_bounded(bar(C::kBarP + 1), j & 1, abort_flag, p.err, kErrMma,
+                                            kTimeoutNs);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                issue_pv(1, j);
+                ptx::tc_commit(bar(C::kBarVE + vs));
+                if (j + 1 < n_tiles) {
+                    issue_qk(1, j + 1);
+                    ptx::tc_commit(bar(C::kBarKE + kn));
+                }
+            }
+            if (ok) {
+                ptx::tc_commit(bar(C::kBarO + 0));
+                ptx::tc_commit(bar(C::kBarO + 1));
+            }
+            // every issued MMA must be finished before TMEM is released
+            int dummy = 0;
+            ptx::tc_commit(bar(C::kBarDrain));
+            ptx::mbar_wait_bounded(bar(C::kBarDrain), 0, (volatile int *)&dummy, nullptr, 0,
+                                   kTimeoutNs);
+        }
+    } else {
+        // ---------------------------------------------------------------- softmax
+        const int t = warp >> 2, wq = warp & 3;
+        const int pos = pos0 + t * kTileM + wq * 32 + lane;
+        const bool row_ok = pos < si.sq;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (uint32_t)t * 128u;
+        const uint32_t tO = tmem + lane_off + 256u + (uint32_t)t * 128u;
+        const long long lim = row_limit(p, si.last_valid, pos);
+        const int kend = lim + 1 < ke ? (int)(lim + 1 > kb ? lim + 1 : kb) : ke;
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = warp_wait(bar(C::kBarS + t), j & 1, abort_flag, p.err, kErrSoftmax);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            uint32_t r[128];
+            ptx::tmem_ld_x128(tS, r);
+            const int nvalid = kend - (kb + j * kBN);
+            float tmax = -INFINITY;
+            if (nvalid >= kBN) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) tmax = fmaxf(tmax, __uint_as_float(r[c]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    float x = c < nvalid ? __uint_as_float(r[c]) : -INFINITY;
+                    r[c] = __float_as_uint(x);
+                    tmax = fmaxf(tmax, x);
+                }
+            }
+            const float m_new = fmaxf(m, tmax * sl2);
+            const bool grow = m_new > m + kRescaleThreshold;  // also true for the first finite max
+            if (__any_sync(0xffffffffu, grow)) {
+                // warp-uniform: TMEM loads and stores are warp-collective
+                const float alpha = grow ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
+                if (j > 0) {
+                    // O_t holds P V of tiles < j (S_t(j) completing implies PV_t(j-1) did)
+#pragma unroll
+                    for (int c0 = 0; c0 < DV; c0 += 32) {
+                        uint32_t o[32];
+                        ptx::tmem_ld_x32(tO + c0, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        ptx::tmem_st_x32(tO + c0, o);
+                    }
+                }
+                l *= alpha;
+                if (grow) m = m_new;
+            }
+            const float mneg = m == -INFINITY ? 0.f : -m;
+            float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = ptx::ex2(fmaf(__uint_as_float(r[2 * c]), sl2, mneg));
+                const float p1 = ptx::ex2(fmaf(__uint_as_float(r[2 * c + 1]), sl2, mneg));
+                rs0 += p0;
+                rs1 += p1;
+                r[c] = ptx::pack2(p0, p1, kBF16);
+            }
+            l += rs0 + rs1;
+            __syncwarp();
+            ptx::tmem_st_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(r));
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(C::kBarP + t));
+        }
+        if (ok && n_tiles > 0) ok = warp_wait(bar(C::kBarO + t), 0, abort_flag, p.err, kErrSoftmax);
+        if (ok) {
+            ptx::tc_fence_after();
+            const bool empty = !(l > 0.f);
+            const float inv = empty ? 0.f : 1.f / l;
+            const float lse = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+            const int row = si.q0 + pos;
+#pragma unroll
+            for (int c0 = 0; c0 < DV; c0 += 32) {
+                uint32_t o[32];
+                if (n_tiles > 0) ptx::tmem_ld_x32(tO + c0, o);
+                else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                if (row_ok) {
+                if constexpr (DIRECT) {
+                    T *dst = (T *)out.ptr + row_offset(p, out, b, si.q0, pos) + (int64_t)h * out.sh + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 v;
+                        v.x = ptx::pack2(__uint_as_float(o[i + 0]) * inv, __uint_as_float(o[i + 1]) * inv, kBF16);
+                        v.y = ptx::pack2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv, kBF16);
+                        v.z = ptx::pack2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv, kBF16);
+                        v.w = ptx::pack2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv, kBF16);
+                        *(uint4 *)(dst + i) = v;
+                    }
+                } else {
+                    float *dst = o_part + (((int64_t)h * p.S + s) * p.total_q + row) * DV + c0;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *(float4 *)(dst + i) = make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                                                           __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+                }
+                }
+                __syncwarp();
+            }
+            if (row_ok) {
+                if constexpr (DIRECT) {
+                    if (lse_out) lse_out[(int64_t)h * p.total_q + row] = lse;
+                } else {
+                    lse_part[((int64_t)h * p.S + s) * p.total_q + row] = lse;
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------------ host
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)f;
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// [rows, H, D] (varlen: rows = total, one batch) or [B][rows][H][D] (dense), box of
+// 64 elements x 128 rows, 128-byte swizzle; out-of-range rows read as zero.
+static bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long long rows, int H,
+                     int B, bool dense) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows <= 0 || t.sr <= 0 || t.sh <= 0) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)(dense ? B : 1)};
+    cuuint64_t strides[3] = {(cuuint64_t)t.sr * 2, (cuuint64_t)t.sh * 2,
+                             (cuuint64_t)(dense ? t.sb : rows * t.sr) * 2};
+    if (dense && t.sb <= 0) return false;
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     4, t.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename T, int DQK, int DV, bool DIRECT>
+static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                              const CUtensorMap &mv, float *o_part, float *lse_part,
+                              const TensorView &out, float *lse_out, cudaStream_t st) {
+    using C = Cfg<DQK, DV>;
+    auto kern = partial_tc_kernel<T, DQK, DV, DIRECT>;
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [&] {
+        attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+    });
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
+    dim3 grid((unsigned)((p.max_sq + kBM - 1) / kBM), (unsigned)p.H, (unsigned)(p.B * p.S));
+    kern<<<grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p, o_part, lse_part, out, lse_out);
+    return cudaGetLastError();
+}
+
+template <typename T, int DQK, int DV>
+static cudaError_t launch_dims(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                               const CUtensorMap &mv, float *o_part, float *lse_part,
+                               const TensorView *out, float *lse_out, cudaStream_t st) {
+    if (out) return launch_cfg<T, DQK, DV, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out, st);
+    return launch_cfg<T, DQK, DV, false>(p, mq, mk, mv, o_part, lse_part, TensorView{}, nullptr, st);
+}
+
+bool partial_tc_supported(const Problem &p, int dtype) {
+    if (dtype != kBF16 && dtype != kF16) return false;
+    if (!((p.d_qk == 64 && p.d_v == 64) || (p.d_qk == 128 && p.d_v == 128) ||
+          (p.d_qk == 192 && p.d_v == 128)))
+        return false;
+    if (p.bm != kBM || p.total_k <= 0 || p.max_sk <= 0 || p.total_q <= 0) return false;
+    if (p.max_sq < kMinQueries) return false;
+    if ((long long)p.B * p.S > 65535 || p.H > 65535) return false;
+    if (encode_fn() == nullptr) return false;
+    return true;
+}
+
+cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, const TensorView &k,
+                              const TensorView &v, float *o_part, float *lse_part,
+                              const TensorView *out, float *lse_out, cudaStream_t st,
+                              bool *launched) {
+    *launched = false;
+    const bool dense = p.cu_q == nullptr;
+    CUtensorMap mq, mk, mv;
+    const long long qrows = dense ? p.max_sq : p.total_q;
+    const long long krows = dense ? p.max_sk : p.total_k;
+    if (!make_map(&mq, q, dtype, p.d_qk, qrows, p.H, p.B, dense) ||
+        !make_map(&mk, k, dtype, p.d_qk, krows, p.H, p.B, dense) ||
+        !make_map(&mv, v, dtype, p.d_v, krows, p.H, p.B, dense))
+        return cudaSuccess;  // not expressible as TMA maps: the caller falls back
+    *launched = true;
+#define SK_TC_DIMS(T)                                                                              \
+    if (p.d_qk == 192) return launch_dims<T, 192, 128>(p, mq, mk, mv, o_part, lse_part, out, lse_out, st); \
+    if (p.d_qk == 128) return launch_dims<T, 128, 128>(p, mq, mk, mv, o_part, lse_part, out, lse_out, st); \
+    return launch_dims<T, 64, 64>(p, mq, mk, mv, o_part, lse_part, out, lse_out, st);
+    if (dtype == kBF16) { SK_TC_DIMS(__nv_bfloat16) }
+    SK_TC_DIMS(__half)
+#undef SK_TC_DIMS
+}
+
+}  // namespace tc
+}  // namespace sk

@@ -167,6 +167,20 @@ cudaError_t launch_partial_simt(const Problem &p, int dtype, const TensorView &q
                                 const TensorView &k, const TensorView &v, float *o_part,
                                 float *lse_part, const TensorView *out, float *lse_out,
                                 cudaStream_t st);
+namespace tc {
+bool partial_tc_supported(const Problem &p, int dtype);
+cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, const TensorView &k,
+                              const TensorView &v, float *o_part, float *lse_part,
+                              const TensorView *out, float *lse_out, cudaStream_t st,
+                              bool *launched);
+}  // namespace tc
+namespace dec {
+bool partial_decode_supported(const Problem &p, int dtype);
+cudaError_t launch_partial_decode(const Problem &p, int dtype, const TensorView &q,
+                                  const TensorView &k, const TensorView &v, float *o_part,
+                                  float *lse_part, const TensorView *out, float *lse_out,
+                                  cudaStream_t st, bool *launched);
+}  // namespace dec
 cudaError_t launch_combine(const Problem &p, int dtype, const float *o_part,
                            const float *lse_part, const int32_t *counts, const TensorView &out,
                            float *lse_out, cudaStream_t st);
