@@ -96,7 +96,7 @@ typedef struct {
     float softmax_scale;         /* 0: 1/sqrt(d_qk) */
 } sk_params;
 
-/* Head-dimension pairs (d_qk, d_v) the kernels are built for. */
+/* Largest split_kv accepted. */
 #define SK_MAX_SPLIT_KV 32
 
 /*
@@ -179,6 +179,10 @@ const char *sk_partial_kernel_name(const sk_params *p, sk_tensor q, sk_tensor k,
 
 /* Human-readable text of a status code. */
 const char *sk_status_string(sk_status s);
+
+/* The CUDA error (a cudaError_t value) behind the most recent SK_ERR_CUDA returned
+ * on the calling thread, 0 if there was none; *name (optional) receives its name. */
+int sk_last_cuda_error(const char **name);
 
 /* Debug: reads (and optionally clears) the device error word that bounded waits
  * set when they give up. SYNCHRONISES the current device. *code = 0: no error. */

@@ -37,7 +37,11 @@ _STATUS = {0: "SK_OK", 1: "SK_ERR_INVALID_ARG", 2: "SK_ERR_UNSUPPORTED", 3: "SK_
 class SplitKVError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {_STATUS.get(status, status)} ({sk_status_string(status)})")
+        detail = ""
+        if status == 4:
+            code, name = sk_last_cuda_error()
+            detail = f"; {name} ({code})"
+        super().__init__(f"{where}: {_STATUS.get(status, status)} ({sk_status_string(status)}{detail})")
 
 
 class _Params(ctypes.Structure):
@@ -90,6 +94,7 @@ def lib():
             L.sk_status_string.argtypes = [ctypes.c_int]
             L.sk_status_string.restype = ctypes.c_char_p
             L.sk_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
+            L.sk_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
             _lib = L
     return _lib
 
@@ -230,6 +235,12 @@ def sk_attn_fwd(p: Params, q, k, v, out, lse_out=None, workspace=None, stream=No
     _ok(lib().sk_attn_fwd(ctypes.byref(p.c()), tensor_desc(q), tensor_desc(k), tensor_desc(v),
                           tensor_desc(out), _ptr(lse_out), _ptr(workspace), ws_bytes,
                           _stream(stream)), "sk_attn_fwd")
+
+
+def sk_last_cuda_error() -> tuple[int, str]:
+    name = ctypes.c_char_p()
+    code = lib().sk_last_cuda_error(ctypes.byref(name))
+    return code, (name.value or b"").decode()
 
 
 def sk_read_device_error(clear: bool = True) -> int:

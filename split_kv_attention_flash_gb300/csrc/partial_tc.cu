@@ -41,9 +41,17 @@ namespace tc {
 constexpr int kBM = 256;         // query rows per CTA
 constexpr int kTileM = 128;      // rows per MMA tile
 constexpr int kBN = 128;         // keys per MMA tile
-constexpr int kThreads = 320;    // 8 softmax warps + producer warp + MMA warp
+constexpr int kThreads = 384;    // softmax warpgroups 0, 1; warpgroup 2: producer, MMA, 2 idle
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Registers are allocated per SM sub-partition: with 12 warps a thread may start with
+// at most 168. Warpgroup 2 gives registers back and the softmax warpgroups take them:
+// 2 * 128 * 208 + 128 * 88 = 384 * 168, exactly the launch's budget.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kControlRegs = 88;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch budget");
 constexpr int kChunkBytes = 128 * 128;  // one 64-column (128-byte) swizzled panel of 128 rows
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.f;  // log2 units: rescale O only when m grows by > 2^8
@@ -99,7 +107,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 template <typename T, int DQK, int DV, bool DIRECT>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, Problem p, float *o_part,
                       float *lse_part, TensorView out, float *lse_out) {
@@ -158,6 +166,8 @@ __global__ void __maxnreg__(200)
     const bool dense = p.cu_q == nullptr;
     const int cb = dense ? b : 0;
 
+    if (warp >= 8) {
+    ptx::regs_dec<kControlRegs>();
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && n_tiles > 0) {
@@ -280,8 +290,10 @@ __global__ void __maxnreg__(200)
             ptx::mbar_wait_bounded(bar(C::kBarDrain), 0, (volatile int *)&dummy, nullptr, 0,
                                    kTimeoutNs);
         }
+    }  // warps 10 and 11 have no role
     } else {
         // ---------------------------------------------------------------- softmax
+        ptx::regs_inc<kSoftmaxRegs>();
         const int t = warp >> 2, wq = warp & 3;
         const int pos = pos0 + t * kTileM + wq * 32 + lane;
         const bool row_ok = pos < si.sq;
@@ -314,23 +326,10 @@ __global__ void __maxnreg__(200)
             }
             const float m_new = fmaxf(m, tmax * sl2);
             const bool grow = m_new > m + kRescaleThreshold;  // also true for the first finite max
-            if (__any_sync(0xffffffffu, grow)) {
-                // warp-uniform: TMEM loads and stores are warp-collective
-                const float alpha = grow ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
-                if (j > 0) {
-                    // O_t holds P V of tiles < j (S_t(j) completing implies PV_t(j-1) did)
-#pragma unroll
-                    for (int c0 = 0; c0 < DV; c0 += 32) {
-                        uint32_t o[32];
-                        ptx::tmem_ld_x32(tO + c0, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        ptx::tmem_st_x32(tO + c0, o);
-                    }
-                }
-                l *= alpha;
-                if (grow) m = m_new;
-            }
+            const bool any_grow = __any_sync(0xffffffffu, grow);
+            const float alpha = grow ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
+            if (grow) m = m_new;
+            l *= alpha;
             const float mneg = m == -INFINITY ? 0.f : -m;
             float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
@@ -342,6 +341,18 @@ __global__ void __maxnreg__(200)
                 r[c] = ptx::pack2(p0, p1, kBF16);
             }
             l += rs0 + rs1;
+            if (any_grow && j > 0) {
+                // warp-uniform (TMEM loads and stores are warp-collective). O_t holds the
+                // P V of tiles < j: S_t(j) completing implies PV_t(j-1) did.
+#pragma unroll
+                for (int c0 = 0; c0 < DV; c0 += 32) {
+                    uint32_t o[32];
+                    ptx::tmem_ld_x32(tO + c0, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    ptx::tmem_st_x32(tO + c0, o);
+                }
+            }
             __syncwarp();
             ptx::tmem_st_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(r));
             ptx::tmem_wait_st();
@@ -403,6 +414,7 @@ __global__ void __maxnreg__(200)
         ptx::tmem_dealloc(tmem, 512);
     }
 }
+static_assert(kLaunchRegs * kThreads <= 65536, "launch registers");
 
 // ------------------------------------------------------------------------ host
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,

@@ -116,7 +116,13 @@ sk::TensorView view(const sk_tensor &t) {
     return sk::TensorView{(char *)t.ptr, t.stride_b, t.stride_row, t.stride_h};
 }
 
-sk_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SK_OK : SK_ERR_CUDA; }
+thread_local int t_last_cuda_error = 0;
+
+sk_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return SK_OK;
+    t_last_cuda_error = (int)e;
+    return SK_ERR_CUDA;
+}
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -140,6 +146,11 @@ WorkspaceLayout layout_for(const sk_params *p, int S) {
 extern "C" {
 
 int sk_version(void) { return 100; }
+
+int sk_last_cuda_error(const char **name) {
+    if (name) *name = t_last_cuda_error ? cudaGetErrorName((cudaError_t)t_last_cuda_error) : "cudaSuccess";
+    return t_last_cuda_error;
+}
 
 const char *sk_status_string(sk_status s) {
     switch (s) {
@@ -187,10 +198,11 @@ sk_status sk_auto_split_kv(const sk_params *p, int *split_kv_out) {
     if (!p || !split_kv_out) return SK_ERR_INVALID_ARG;
     if (p->split_kv > 0) return sk_choose_split_kv(p, 1, split_kv_out);
     int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
-        return SK_ERR_CUDA;
+        return cuda_status(e);
     }
     return sk_choose_split_kv(p, sms, split_kv_out);
 }
