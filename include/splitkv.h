@@ -150,6 +150,31 @@ sk_status sk_combine(const sk_params *p, const float *o_part, const float *lse_p
 sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v, sk_tensor out,
                       float *lse_out, void *workspace, size_t workspace_bytes, sk_stream stream);
 
+/* Bytes of scratch that sk_attn_fwd_static keeps inside the library (32 MiB). */
+#define SK_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * sk_attn_fwd_static -- sk_attn_fwd for callers that cannot allocate device memory.
+ * The pages have no counterpart: this call exists for users of this library whose
+ * device memory is planned once up front (a serving loop that must not allocate per
+ * request) or whose host framework owns every allocation and gives a plugin no
+ * allocator, so they cannot hand sk_attn_fwd a workspace. It computes exactly what
+ * sk_attn_fwd computes, with the workspace taken from a file-scope device array of
+ * SK_STATIC_SCRATCH_BYTES that every GPU loading the library holds until exit.
+ *   - The caller still passes Q, K, V, out and (optionally) lse_out.
+ *   - Problems whose sk_workspace_bytes() exceeds SK_STATIC_SCRATCH_BYTES are
+ *     rejected with SK_ERR_WORKSPACE before anything is launched.
+ *   - It calls no cudaMalloc / cudaFree and no allocating library routine.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array and leaves its contents behind;
+ *     nothing in it has to start at zero (each call writes what it later reads).
+ *     Calls that overlap on the GPU (other streams, other threads) race on it.
+ */
+sk_status sk_attn_fwd_static(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
+                             sk_tensor out, float *lse_out, sk_stream stream);
+
 /* Bytes of workspace sk_attn_fwd needs for these parameters (0 when S == 1).
  * Resolving split_kv = 0 reads the current device's SM count. */
 sk_status sk_workspace_bytes(const sk_params *p, size_t *bytes);

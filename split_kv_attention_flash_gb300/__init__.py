@@ -237,6 +237,21 @@ def sk_attn_fwd(p: Params, q, k, v, out, lse_out=None, workspace=None, stream=No
                           _stream(stream)), "sk_attn_fwd")
 
 
+SK_STATIC_SCRATCH_BYTES = 32 << 20   # mirrors include/splitkv.h
+
+
+def sk_attn_fwd_static(p: Params, q, k, v, out, lse_out=None, stream=None):
+    """sk_attn_fwd without a workspace argument, for callers that cannot allocate:
+    the library's own fixed scratch array (SK_STATIC_SCRATCH_BYTES per GPU) holds the
+    split partials. Problems that need more scratch raise SK_ERR_WORKSPACE."""
+    L = lib()
+    fn = L.sk_attn_fwd_static
+    fn.argtypes = [ctypes.POINTER(_Params), _Tensor, _Tensor, _Tensor, _Tensor, ctypes.c_void_p,
+                   ctypes.c_void_p]
+    _ok(fn(ctypes.byref(p.c()), tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out),
+           _ptr(lse_out), _stream(stream)), "sk_attn_fwd_static")
+
+
 def sk_last_cuda_error() -> tuple[int, str]:
     name = ctypes.c_char_p()
     code = lib().sk_last_cuda_error(ctypes.byref(name))
