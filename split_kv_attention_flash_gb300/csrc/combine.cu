@@ -1,102 +1,158 @@
 // combine.cu -- NaN-safe f32 merge of split partials ([P1] Technical details:
 // NaN-safe merge (computeFinalAttentionStage), f32 merge for f16/bf16).
 //
-// One warp merges one (head, query row). Lane s < count holds L_s; a warp max and
-// sum give m and sum_s w_s; then every partial row O_s (d_v f32, contiguous) is read
-// once with 16-byte loads, weighted and summed. Splits s >= count are never read.
+// Per (head, row), over the splits s < count (the others are never read):
+//   m = max(max_s L_s, lowest finite);  w_s = exp(L_s - m)
+//   O = sum_s w_s O_s / max(sum_s w_s, 1);   LSE = m + log(sum_s w_s)  (or -inf)
+//
 // The pass is HBM-bound: it reads count * (4 d_v + 4) bytes and writes d_v
-// storage-type elements (+ 4 bytes of LSE) per (head, row).
+// storage-type elements (+ 4 bytes of LSE) per (head, row). A CTA merges 32
+// consecutive rows of one head (one contiguous run of every (head, split) plane):
+//   * every warp reads the counts of its 4 rows and at once issues the 16-byte
+//     loads of up to kPrefetch partial rows each, so that a lane has up to 16
+//     independent loads in flight before any arithmetic;
+//   * meanwhile warp 0 (one lane per row) reads the L_s, forms m and the weights
+//     into shared memory and writes the final LSE, all coalesced;
+//   * after one barrier every warp weights, sums, scales and stores its rows.
 #include <float.h>
 
 #include "sk_common.cuh"
 
 namespace sk {
 
-constexpr int kCombineWarps = 8;
+namespace {
+constexpr int kWarps = 8;
+constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerCta = kWarps * kRowsPerWarp;  // 32: one lane per row in warp 0
+constexpr int kPrefetch = 4;                          // partial rows per row loaded up front
+constexpr int kMaxSplits = 32;
+}  // namespace
 
 template <typename TO, int DV>
-__global__ void __launch_bounds__(kCombineWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32)
     combine_kernel(Problem p, const float *__restrict__ o_part, const float *__restrict__ lse_part,
                    const int32_t *__restrict__ counts, TensorView out, float *__restrict__ lse_out,
                    int row_blocks) {
     static_assert(DV % 4 == 0 && DV / 4 <= 32, "one float4 per lane");
     constexpr int kLanes = DV / 4;
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+    __shared__ float sW[kMaxSplits][kRowsPerCta];
+    __shared__ float sInv[kRowsPerCta];
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.y;
     const int b = blockIdx.x / row_blocks;
-    const int pos = (blockIdx.x % row_blocks) * kCombineWarps + warp;
+    const int pos0 = (blockIdx.x % row_blocks) * kRowsPerCta;
     const SeqInfo si = seq_info(p, b);
-    if (pos >= si.sq) return;
-    const int row = si.q0 + pos;
+    if (pos0 >= si.sq) return;
+    const int nrows = min(kRowsPerCta, si.sq - pos0);
     const int S = p.S;
+    const int64_t plane = (int64_t)p.total_q;          // rows per (head, split) plane
+    const int row0 = si.q0 + pos0;
+    const float *obase = o_part + ((int64_t)h * S * plane + row0) * DV + lane * 4;
 
-    int count = __ldg(counts + row);
-    count = count < 1 ? 1 : (count > S ? S : count);
-
-    // m = max(max_s L_s, lowest finite); w_s = exp(L_s - m)
-    const float *lrow = lse_part + (int64_t)h * S * p.total_q + row;
-    float l = lane < count ? __ldg(lrow + (int64_t)lane * p.total_q) : -INFINITY;
-    float m = fmaxf(group_max<32>(l), -FLT_MAX);
-    float w = lane < count ? expf(l - m) : 0.f;
-    float wsum = group_sum<32>(w);
-
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float *orow = o_part + ((int64_t)h * S * p.total_q + row) * DV + lane * 4;
-    const int64_t split_stride = (int64_t)p.total_q * DV;
-    int s = 0;
-    for (; s + 4 <= count; s += 4) {  // four independent 16-byte loads in flight
-        float4 o[4];
+    // ---- issue this warp's partial-row loads (they depend only on the counts)
+    int cnt[kRowsPerWarp];
+    float4 pre[kRowsPerWarp][kPrefetch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            o[u] = lane < kLanes ? __ldg((const float4 *)(orow + (s + u) * split_stride))
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int r = warp * kRowsPerWarp + i;
+        int c = r < nrows ? __ldg(counts + row0 + r) : 0;
+        cnt[i] = c < 0 ? 0 : (c > S ? S : c);
+        if (r < nrows && cnt[i] < 1) cnt[i] = 1;
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int r = warp * kRowsPerWarp + i;
+#pragma unroll
+        for (int s = 0; s < kPrefetch; ++s)
+            pre[i][s] = (s < cnt[i] && lane < kLanes)
+                            ? __ldg((const float4 *)(obase + ((int64_t)s * plane + r) * DV))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
+    // ---- weights: warp 0, one lane per row
+    if (warp == 0) {
+        const int r = lane;
+        int c = 0;
+        if (r < nrows) {
+            c = __ldg(counts + row0 + r);
+            c = c < 1 ? 1 : (c > S ? S : c);
+        }
+        const float *lrow = lse_part + (int64_t)h * S * plane + row0 + r;
+        float m = -FLT_MAX;  // max(max_s L_s, lowest finite)
+        for (int s = 0; s < c; ++s) {
+            const float l = __ldg(lrow + s * plane);
+            sW[s][r] = l;
+            m = fmaxf(m, l);
+        }
+        float wsum = 0.f;
+        for (int s = 0; s < c; ++s) {
+            const float w = expf(sW[s][r] - m);
+            sW[s][r] = w;
+            wsum += w;
+        }
+        sInv[r] = 1.f / fmaxf(wsum, 1.f);  // the max only binds when every split is empty
+        if (lse_out && r < nrows)
+            lse_out[(int64_t)h * plane + row0 + r] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+    }
+    __syncthreads();
+
+    // ---- weighted sums and stores
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int r = warp * kRowsPerWarp + i;
+        if (r >= nrows) break;  // warp-uniform
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < kPrefetch; ++s) {
+            if (s < cnt[i]) {
+                const float w = sW[s][r];
+                acc.x = fmaf(w, pre[i][s].x, acc.x);
+                acc.y = fmaf(w, pre[i][s].y, acc.y);
+                acc.z = fmaf(w, pre[i][s].z, acc.z);
+                acc.w = fmaf(w, pre[i][s].w, acc.w);
+            }
+        }
+        for (int s = kPrefetch; s < cnt[i]; ++s) {  // more splits than prefetched
+            const float4 o = lane < kLanes
+                                 ? __ldg((const float4 *)(obase + ((int64_t)s * plane + r) * DV))
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float ws = __shfl_sync(0xffffffffu, w, s + u);
-            acc.x = fmaf(ws, o[u].x, acc.x);
-            acc.y = fmaf(ws, o[u].y, acc.y);
-            acc.z = fmaf(ws, o[u].z, acc.z);
-            acc.w = fmaf(ws, o[u].w, acc.w);
+            const float w = sW[s][r];
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+        }
+        const float inv = sInv[r];
+        if (lane < kLanes) {
+            TO *dst = (TO *)out.ptr + row_offset(p, out, b, si.q0, pos0 + r) + (int64_t)h * out.sh +
+                      lane * 4;
+            if constexpr (sizeof(TO) == 4) {
+                *(float4 *)dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            } else {
+                TO v[4] = {from_f32<TO>(acc.x * inv), from_f32<TO>(acc.y * inv),
+                           from_f32<TO>(acc.z * inv), from_f32<TO>(acc.w * inv)};
+                *(uint2 *)dst = *(const uint2 *)v;
+            }
         }
     }
-    for (; s < count; ++s) {
-        float4 o = lane < kLanes ? __ldg((const float4 *)(orow + s * split_stride))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-        float ws = __shfl_sync(0xffffffffu, w, s);
-        acc.x = fmaf(ws, o.x, acc.x);
-        acc.y = fmaf(ws, o.y, acc.y);
-        acc.z = fmaf(ws, o.z, acc.z);
-        acc.w = fmaf(ws, o.w, acc.w);
-    }
-    const float denom = fmaxf(wsum, 1.f);  // only binds when every split is empty
-
-    if (lane < kLanes) {
-        TO *dst = (TO *)out.ptr + row_offset(p, out, b, si.q0, pos) + (int64_t)h * out.sh + lane * 4;
-        if constexpr (sizeof(TO) == 4) {
-            *(float4 *)dst = make_float4(acc.x / denom, acc.y / denom, acc.z / denom, acc.w / denom);
-        } else {
-            TO v[4] = {from_f32<TO>(acc.x / denom), from_f32<TO>(acc.y / denom),
-                       from_f32<TO>(acc.z / denom), from_f32<TO>(acc.w / denom)};
-            *(uint2 *)dst = *(const uint2 *)v;
-        }
-    }
-    if (lse_out && lane == 0)
-        lse_out[(int64_t)h * p.total_q + row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
 template <typename TO>
 static cudaError_t launch_dv(const Problem &p, const float *o_part, const float *lse_part,
                              const int32_t *counts, const TensorView &out, float *lse_out,
                              cudaStream_t st) {
-    const int row_blocks = (p.max_sq + kCombineWarps - 1) / kCombineWarps;
-    dim3 grid((unsigned)((long long)row_blocks * p.B), (unsigned)p.H);
+    if (p.S > kMaxSplits) return cudaErrorInvalidValue;
+    const int row_blocks = (p.max_sq + kRowsPerCta - 1) / kRowsPerCta;
+    const long long nx = (long long)row_blocks * p.B;
+    if (nx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    dim3 grid((unsigned)nx, (unsigned)p.H);
     if (p.d_v == 128)
-        combine_kernel<TO, 128><<<grid, kCombineWarps * 32, 0, st>>>(p, o_part, lse_part, counts,
-                                                                      out, lse_out, row_blocks);
+        combine_kernel<TO, 128><<<grid, kWarps * 32, 0, st>>>(p, o_part, lse_part, counts, out,
+                                                              lse_out, row_blocks);
     else if (p.d_v == 64)
-        combine_kernel<TO, 64><<<grid, kCombineWarps * 32, 0, st>>>(p, o_part, lse_part, counts,
-                                                                     out, lse_out, row_blocks);
+        combine_kernel<TO, 64><<<grid, kWarps * 32, 0, st>>>(p, o_part, lse_part, counts, out,
+                                                             lse_out, row_blocks);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

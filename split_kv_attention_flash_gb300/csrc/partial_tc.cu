@@ -312,18 +312,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[128];
             ptx::tmem_ld_x128(tS, r);
             const int nvalid = kend - (kb + j * kBN);
-            float tmax = -INFINITY;
-            if (nvalid >= kBN) {
+            if (nvalid < kBN) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) tmax = fmaxf(tmax, __uint_as_float(r[c]));
-            } else {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    float x = c < nvalid ? __uint_as_float(r[c]) : -INFINITY;
-                    r[c] = __float_as_uint(x);
-                    tmax = fmaxf(tmax, x);
-                }
+                for (int c = 0; c < 128; ++c)
+                    if (c >= nvalid) r[c] = __float_as_uint(-INFINITY);
             }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(r[c + u]));
+            }
+            const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             const float m_new = fmaxf(m, tmax * sl2);
             const bool grow = m_new > m + kRescaleThreshold;  // also true for the first finite max
             const bool any_grow = __any_sync(0xffffffffu, grow);
@@ -331,16 +331,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (grow) m = m_new;
             l *= alpha;
             const float mneg = m == -INFINITY ? 0.f : -m;
-            float rs0 = 0.f, rs1 = 0.f;
+            // p = 2^(s * scale * log2 e - m), two columns per packed FMA
+            const uint64_t sc2 = ptx::f2pack(sl2, sl2), mn2 = ptx::f2pack(mneg, mneg);
+            uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const float p0 = ptx::ex2(fmaf(__uint_as_float(r[2 * c]), sl2, mneg));
-                const float p1 = ptx::ex2(fmaf(__uint_as_float(r[2 * c + 1]), sl2, mneg));
-                rs0 += p0;
-                rs1 += p1;
-                r[c] = ptx::pack2(p0, p1, kBF16);
+                float a, bq;
+                ptx::f2unpack(ptx::ffma2(ptx::f2pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])),
+                                         sc2, mn2),
+                              a, bq);
+                a = ptx::ex2(a);
+                bq = ptx::ex2(bq);
+                sum2[c & 1] = ptx::fadd2(sum2[c & 1], ptx::f2pack(a, bq));
+                r[c] = ptx::pack2(a, bq, kBF16);
             }
-            l += rs0 + rs1;
+            {
+                float s0, s1, s2, s3;
+                ptx::f2unpack(sum2[0], s0, s1);
+                ptx::f2unpack(sum2[1], s2, s3);
+                l += (s0 + s1) + (s2 + s3);
+            }
             if (any_grow && j > 0) {
                 // warp-uniform (TMEM loads and stores are warp-collective). O_t holds the
                 // P V of tiles < j: S_t(j) completing implies PV_t(j-1) did.

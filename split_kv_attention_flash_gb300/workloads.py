@@ -139,5 +139,9 @@ DECODE = Workload("decode bf16 (B32 H32 Sq1, Sk ~ U[4096, 131072], D128)", H=32,
                   seqlens_q=(1,) * 32, seqlens_k=decode_lengths(32, 4096, 131072, 4),
                   d_qk=128, d_v=128, dtype="bf16", seed=4, n_per_block=128, split_kv=0)
 
+# the target shape with D_QK = D_V = 128, for comparing the head-dim configurations
+TARGET_D128 = TARGET_SHAPE.with_(name="varlen prefill bf16 Sq4096 Sk42700 H12 D128/128 non-causal",
+                                 d_qk=128, d_v=128)
+
 ALL = {"tiny": TINY_CAUSAL, "noncausal": NONCAUSAL_BF16, "masked": MASKED_F16,
-       "varlen": LONG_VARLEN, "target": TARGET_SHAPE, "decode": DECODE}
+       "varlen": LONG_VARLEN, "target": TARGET_SHAPE, "decode": DECODE, "target_d128": TARGET_D128}
