@@ -6,8 +6,15 @@
 //   O = sum_s w_s O_s / max(sum_s w_s, 1);   LSE = m + log(sum_s w_s)  (or -inf)
 //
 // The pass is HBM-bound: it reads count * (4 d_v + 4) bytes and writes d_v
-// storage-type elements (+ 4 bytes of LSE) per (head, row). A CTA merges 32
-// consecutive rows of one head (one contiguous run of every (head, split) plane):
+// storage-type elements (+ 4 bytes of LSE) per (head, row).
+//
+// combine_bulk_kernel (S <= 8): a CTA merges 32 consecutive rows of one head. For a
+// (head, split) plane those rows are one contiguous chunk of 32 * d_v floats, so one
+// thread issues one bulk asynchronous copy per split into shared memory (splits up
+// to the largest count of the 32 rows) while warp 0 forms the weights; then every
+// warp merges 8 rows out of shared memory.
+//
+// combine_kernel (any S <= 32): a CTA merges 32 consecutive rows of one head:
 //   * every warp reads the counts of its 4 rows and at once issues the 16-byte
 //     loads of up to kPrefetch partial rows each, so that a lane has up to 16
 //     independent loads in flight before any arithmetic;
@@ -16,7 +23,10 @@
 //   * after one barrier every warp weights, sums, scales and stores its rows.
 #include <float.h>
 
+#include <mutex>
+
 #include "sk_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace sk {
 
@@ -138,11 +148,152 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 }
 
+namespace {
+constexpr int kBulkRows = 32;
+constexpr int kBulkThreads = 128;
+constexpr int kBulkMaxSplits = 8;
+constexpr uint64_t kBulkTimeoutNs = 1000000000ull;
+}  // namespace
+
+template <typename TO, int DV>
+__global__ void __launch_bounds__(kBulkThreads)
+    combine_bulk_kernel(Problem p, const float *__restrict__ o_part,
+                        const float *__restrict__ lse_part, const int32_t *__restrict__ counts,
+                        TensorView out, float *__restrict__ lse_out, int row_blocks) {
+    static_assert(DV % 4 == 0 && DV / 4 <= 32, "one float4 per lane");
+    constexpr int kLanes = DV / 4;
+    extern __shared__ __align__(128) uint8_t sO_raw[];   // [split][32 rows][DV] f32
+    __shared__ __align__(8) uint64_t sBar;
+    __shared__ float sW[kBulkMaxSplits][kBulkRows];
+    __shared__ float sInv[kBulkRows];
+    __shared__ int sCnt[kBulkRows];
+    __shared__ int sMax;
+    __shared__ volatile int sAbort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.y;
+    const int b = blockIdx.x / row_blocks;
+    const int pos0 = (blockIdx.x % row_blocks) * kBulkRows;
+    const SeqInfo si = seq_info(p, b);
+    if (pos0 >= si.sq) return;
+    const int nrows = min(kBulkRows, si.sq - pos0);
+    const int S = p.S;
+    const int64_t plane = (int64_t)p.total_q;
+    const int row0 = si.q0 + pos0;
+    const uint32_t bar = ptx::smem_u32(&sBar);
+    const float *sO = (const float *)sO_raw;
+
+    if (warp == 0) {
+        int c = 0;
+        if (lane < nrows) {
+            c = __ldg(counts + row0 + lane);
+            c = c < 1 ? 1 : (c > S ? S : c);
+        }
+        sCnt[lane] = c;
+        int cmax = c;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+        if (lane == 0) {
+            sMax = cmax;
+            sAbort = 0;
+            ptx::mbar_init(bar, 1);
+            ptx::fence_mbar_init();
+        }
+    }
+    __syncthreads();
+    const int nsplit = sMax;
+    if (tid == 0) {
+        const uint32_t chunk = (uint32_t)nrows * DV * 4;
+        ptx::mbar_arrive_expect_tx(bar, chunk * (uint32_t)nsplit);
+        for (int sp = 0; sp < nsplit; ++sp)
+            ptx::bulk_load(ptx::smem_u32(sO_raw) + (uint32_t)sp * kBulkRows * DV * 4,
+                           o_part + (((int64_t)h * S + sp) * plane + row0) * DV, chunk, bar);
+    }
+    if (warp == 0) {
+        // weights, one lane per row: m = max(max_s L_s, lowest finite), w_s = exp(L_s - m)
+        const int r = lane, c = sCnt[r];
+        const float *lrow = lse_part + (int64_t)h * S * plane + row0 + r;
+        float l[kBulkMaxSplits];
+        float m = -FLT_MAX;
+#pragma unroll
+        for (int sp = 0; sp < kBulkMaxSplits; ++sp) {
+            l[sp] = sp < c ? __ldg(lrow + sp * plane) : -INFINITY;
+            m = fmaxf(m, l[sp]);
+        }
+        float wsum = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kBulkMaxSplits; ++sp) {
+            const float w = sp < c ? expf(l[sp] - m) : 0.f;
+            sW[sp][r] = w;
+            wsum += w;
+        }
+        sInv[r] = 1.f / fmaxf(wsum, 1.f);  // the max only binds when every split is empty
+        if (lse_out && r < nrows)
+            lse_out[(int64_t)h * plane + row0 + r] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+    }
+    __syncthreads();
+    if (!ptx::mbar_wait_bounded(bar, 0, &sAbort, p.err, 0x301, kBulkTimeoutNs)) return;
+#pragma unroll
+    for (int i = 0; i < kBulkRows / 4; ++i) {
+        const int r = warp * (kBulkRows / 4) + i;
+        if (r >= nrows) break;  // warp-uniform
+        const int c = sCnt[r];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < kLanes) {
+            for (int sp = 0; sp < c; ++sp) {
+                const float4 o = *(const float4 *)(sO + ((size_t)sp * kBulkRows + r) * DV + lane * 4);
+                const float w = sW[sp][r];
+                acc.x = fmaf(w, o.x, acc.x);
+                acc.y = fmaf(w, o.y, acc.y);
+                acc.z = fmaf(w, o.z, acc.z);
+                acc.w = fmaf(w, o.w, acc.w);
+            }
+            const float inv = sInv[r];
+            TO *dst = (TO *)out.ptr + row_offset(p, out, b, si.q0, pos0 + r) + (int64_t)h * out.sh +
+                      lane * 4;
+            if constexpr (sizeof(TO) == 4) {
+                *(float4 *)dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            } else {
+                TO v[4] = {from_f32<TO>(acc.x * inv), from_f32<TO>(acc.y * inv),
+                           from_f32<TO>(acc.z * inv), from_f32<TO>(acc.w * inv)};
+                *(uint2 *)dst = *(const uint2 *)v;
+            }
+        }
+    }
+}
+
+template <typename TO, int DV>
+static cudaError_t launch_bulk(const Problem &p, const float *o_part, const float *lse_part,
+                               const int32_t *counts, const TensorView &out, float *lse_out,
+                               cudaStream_t st) {
+    auto kern = combine_bulk_kernel<TO, DV>;
+    constexpr int kMaxSmem = kBulkMaxSplits * kBulkRows * DV * 4;
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [&] {
+        attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    });
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
+    const int row_blocks = (p.max_sq + kBulkRows - 1) / kBulkRows;
+    const long long nx = (long long)row_blocks * p.B;
+    if (nx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int smem = p.S * kBulkRows * DV * 4;
+    kern<<<dim3((unsigned)nx, (unsigned)p.H), kBulkThreads, smem, st>>>(p, o_part, lse_part, counts,
+                                                                       out, lse_out, row_blocks);
+    return cudaGetLastError();
+}
+
 template <typename TO>
 static cudaError_t launch_dv(const Problem &p, const float *o_part, const float *lse_part,
                              const int32_t *counts, const TensorView &out, float *lse_out,
                              cudaStream_t st) {
     if (p.S > kMaxSplits) return cudaErrorInvalidValue;
+    if (p.S <= kBulkMaxSplits) {
+        if (p.d_v == 128) return launch_bulk<TO, 128>(p, o_part, lse_part, counts, out, lse_out, st);
+        if (p.d_v == 64) return launch_bulk<TO, 64>(p, o_part, lse_part, counts, out, lse_out, st);
+    }
     const int row_blocks = (p.max_sq + kRowsPerCta - 1) / kRowsPerCta;
     const long long nx = (long long)row_blocks * p.B;
     if (nx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

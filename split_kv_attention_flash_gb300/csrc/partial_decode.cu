@@ -58,8 +58,9 @@ __device__ __forceinline__ void widen8(uint4 u, float (&f)[8]) {
     for (int i = 0; i < 8; ++i) f[i] = to_f32(h[i]);
 }
 
-template <typename T, int DQK, int DV, bool DIRECT>
-__global__ void __launch_bounds__(kThreads)
+// Up to 4 query rows the kernel fits two CTAs per SM (registers <= 112).
+template <typename T, int DQK, int DV, bool DIRECT, int NR>
+__global__ void __launch_bounds__(kThreads, NR <= 4 ? 2 : 1)
     partial_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           Problem p, TensorView q, float *o_part, float *lse_part, TensorView out,
                           float *lse_out) {
@@ -68,7 +69,9 @@ __global__ void __launch_bounds__(kThreads)
     const int h = blockIdx.y;
     const int s = blockIdx.x % p.S, b = blockIdx.x / p.S;
     const SeqInfo si = seq_info(p, b);
-    const int R = si.sq < kMaxRows ? si.sq : kMaxRows;
+    // NR (a power of two >= every sequence's query count) rows are computed; rows at or
+    // past this sequence's count are masked out and never stored
+    const int R = si.sq < NR ? si.sq : NR;
     if (R <= 0) return;
     int kb, ke;
     split_key_range(p, si.sq, si.last_valid, 0, s, kb, ke);
@@ -93,10 +96,12 @@ __global__ void __launch_bounds__(kThreads)
         ptx::fence_mbar_init();
     }
     // queries, widened and pre-scaled into base-2 score units
-    for (int e = threadIdx.x; e < R * DQK; e += kThreads) {
+    for (int e = threadIdx.x; e < NR * DQK; e += kThreads) {
         const int r = e / DQK, d = e % DQK;
-        const T *src = (const T *)q.ptr + row_offset(p, q, b, si.q0, r) + (int64_t)h * q.sh + d;
-        sq[r * DQK + d] = to_f32(*src) * p.scale_log2;
+        float x = 0.f;
+        if (r < R)
+            x = to_f32(((const T *)q.ptr)[row_offset(p, q, b, si.q0, r) + (int64_t)h * q.sh + d]);
+        sq[r * DQK + d] = x * p.scale_log2;
     }
     __syncthreads();
 
@@ -139,19 +144,20 @@ __global__ void __launch_bounds__(kThreads)
     // ------------------------------------------------------------------ compute
     const int kl = lane >> 2;          // key of the warp's 8 in this tile
     const int dq = lane & 3;           // quarter of the dot product
-    int kend[kMaxRows];
+    int kend[NR];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
-        int e = ke;
+    for (int r = 0; r < NR; ++r) {
+        int e = kb;  // rows past the sequence see nothing
         if (r < R) {
+            e = ke;
             const long long lim = row_limit(p, si.last_valid, r);
             if (lim + 1 < e) e = (int)(lim + 1 > kb ? lim + 1 : kb);
         }
         kend[r] = e;
     }
-    float m[kMaxRows], l[kMaxRows], acc[kMaxRows][C::kVPer];
+    float m[NR], l[NR], acc[NR][C::kVPer];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
+    for (int r = 0; r < NR; ++r) {
         m[r] = -INFINITY;
         l[r] = 0.f;
 #pragma unroll
@@ -187,30 +193,27 @@ __global__ void __launch_bounds__(kThreads)
         const int kidx = kb + j * kKT + key;           // key index in the sequence
 
         // scores of this lane's key for every query (quarter dot + 2 shuffles)
-        float sc[kMaxRows];
+        float sc[NR];
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) sc[r] = 0.f;
+        for (int r = 0; r < NR; ++r) sc[r] = 0.f;
 #pragma unroll
         for (int c8 = 0; c8 < C::kDPer / 8; ++c8) {
             const int d0 = dq * C::kDPer + c8 * 8;
             float kf[8];
             widen8<T>(*(const uint4 *)(kt + swz(key, d0, kKT)), kf);
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-                if (r < R) {
-                    const float4 qa = *(const float4 *)(sq + r * DQK + d0);
-                    const float4 qb = *(const float4 *)(sq + r * DQK + d0 + 4);
-                    sc[r] = fmaf(qa.x, kf[0], sc[r]); sc[r] = fmaf(qa.y, kf[1], sc[r]);
-                    sc[r] = fmaf(qa.z, kf[2], sc[r]); sc[r] = fmaf(qa.w, kf[3], sc[r]);
-                    sc[r] = fmaf(qb.x, kf[4], sc[r]); sc[r] = fmaf(qb.y, kf[5], sc[r]);
-                    sc[r] = fmaf(qb.z, kf[6], sc[r]); sc[r] = fmaf(qb.w, kf[7], sc[r]);
-                }
+            for (int r = 0; r < NR; ++r) {
+                const float4 qa = *(const float4 *)(sq + r * DQK + d0);
+                const float4 qb = *(const float4 *)(sq + r * DQK + d0 + 4);
+                sc[r] = fmaf(qa.x, kf[0], sc[r]); sc[r] = fmaf(qa.y, kf[1], sc[r]);
+                sc[r] = fmaf(qa.z, kf[2], sc[r]); sc[r] = fmaf(qa.w, kf[3], sc[r]);
+                sc[r] = fmaf(qb.x, kf[4], sc[r]); sc[r] = fmaf(qb.y, kf[5], sc[r]);
+                sc[r] = fmaf(qb.z, kf[6], sc[r]); sc[r] = fmaf(qb.w, kf[7], sc[r]);
             }
         }
-        float pr[kMaxRows];
+        float pr[NR];
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
-            if (r >= R) { pr[r] = 0.f; continue; }
+        for (int r = 0; r < NR; ++r) {
             float x = sc[r];
             x += __shfl_xor_sync(0xffffffffu, x, 1);
             x += __shfl_xor_sync(0xffffffffu, x, 2);
@@ -251,12 +254,10 @@ __global__ void __launch_bounds__(kThreads)
                 for (int i = 0; i < C::kVPer; ++i) vf[i] = to_f32(hh[i]);
             }
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-                if (r < R) {
-                    const float pk = __shfl_sync(0xffffffffu, pr[r], 4 * k8);
+            for (int r = 0; r < NR; ++r) {
+                const float pk = __shfl_sync(0xffffffffu, pr[r], 4 * k8);
 #pragma unroll
-                    for (int i = 0; i < C::kVPer; ++i) acc[r][i] = fmaf(pk, vf[i], acc[r][i]);
-                }
+                for (int i = 0; i < C::kVPer; ++i) acc[r][i] = fmaf(pk, vf[i], acc[r][i]);
             }
         }
         __syncwarp();
@@ -265,20 +266,20 @@ __global__ void __launch_bounds__(kThreads)
 
     // ------------------------------------------------------- merge of the 8 warps
     __syncthreads();  // (1) every warp left the loop; the ring is free
-    float *mm = (float *)gring;                                 // [8][16] max
-    float *ll = mm + kComputeWarps * kMaxRows;                  // [8][16] sum
-    float *aa = ll + kComputeWarps * kMaxRows;                  // [8][16][DV]
+    float *mm = (float *)gring;                  // [8][NR] max
+    float *ll = mm + kComputeWarps * NR;         // [8][NR] sum
+    float *aa = ll + kComputeWarps * NR;         // [8][NR][DV]
     if (ok) {
 #pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) {
+        for (int r = 0; r < NR; ++r) {
             if (r >= R) continue;
             if (lane == 0) {
-                mm[warp * kMaxRows + r] = m[r];
-                ll[warp * kMaxRows + r] = l[r];
+                mm[warp * NR + r] = m[r];
+                ll[warp * NR + r] = l[r];
             }
 #pragma unroll
             for (int i = 0; i < C::kVPer; ++i)
-                aa[(warp * kMaxRows + r) * DV + lane * C::kVPer + i] = acc[r][i];
+                aa[(warp * NR + r) * DV + lane * C::kVPer + i] = acc[r][i];
         }
     }
     __syncthreads();  // (2)
@@ -287,14 +288,14 @@ __global__ void __launch_bounds__(kThreads)
         const int r = e / DV, d = e % DV;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, mm[w * kMaxRows + r]);
+        for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, mm[w * NR + r]);
         const float Mu = M == -INFINITY ? 0.f : M;
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < kComputeWarps; ++w) {
-            const float f = ptx::ex2(mm[w * kMaxRows + r] - Mu);
-            L = fmaf(ll[w * kMaxRows + r], f, L);
-            O = fmaf(aa[(w * kMaxRows + r) * DV + d], f, O);
+            const float f = ptx::ex2(mm[w * NR + r] - Mu);
+            L = fmaf(ll[w * NR + r], f, L);
+            O = fmaf(aa[(w * NR + r) * DV + d], f, O);
         }
         const bool emp = !(L > 0.f);
         const float o = emp ? 0.f : O / L;
@@ -349,12 +350,12 @@ static bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int DQK, int DV, bool DIRECT>
-static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mk, const CUtensorMap &mv,
-                              const TensorView &q, float *o_part, float *lse_part,
-                              const TensorView &out, float *lse_out, cudaStream_t st) {
+template <typename T, int DQK, int DV, bool DIRECT, int NR>
+static cudaError_t launch_rows(const Problem &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                               const TensorView &q, float *o_part, float *lse_part,
+                               const TensorView &out, float *lse_out, cudaStream_t st) {
     using C = Cfg<DQK, DV>;
-    auto kern = partial_decode_kernel<T, DQK, DV, DIRECT>;
+    auto kern = partial_decode_kernel<T, DQK, DV, DIRECT, NR>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -367,6 +368,17 @@ static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mk, const CUt
     dim3 grid((unsigned)(p.B * p.S), (unsigned)p.H);
     kern<<<grid, kThreads, C::kSmemBytes, st>>>(mk, mv, p, q, o_part, lse_part, out, lse_out);
     return cudaGetLastError();
+}
+
+template <typename T, int DQK, int DV, bool DIRECT>
+static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                              const TensorView &q, float *o_part, float *lse_part,
+                              const TensorView &out, float *lse_out, cudaStream_t st) {
+    if (p.max_sq <= 1) return launch_rows<T, DQK, DV, DIRECT, 1>(p, mk, mv, q, o_part, lse_part, out, lse_out, st);
+    if (p.max_sq <= 2) return launch_rows<T, DQK, DV, DIRECT, 2>(p, mk, mv, q, o_part, lse_part, out, lse_out, st);
+    if (p.max_sq <= 4) return launch_rows<T, DQK, DV, DIRECT, 4>(p, mk, mv, q, o_part, lse_part, out, lse_out, st);
+    if (p.max_sq <= 8) return launch_rows<T, DQK, DV, DIRECT, 8>(p, mk, mv, q, o_part, lse_part, out, lse_out, st);
+    return launch_rows<T, DQK, DV, DIRECT, 16>(p, mk, mv, q, o_part, lse_part, out, lse_out, st);
 }
 
 template <typename T, int DQK, int DV>
