@@ -1,0 +1,84 @@
+"""Host-side logic of bench.py (no GPU): the FLOP and byte counts it reports, and
+its multi-rank path -- max-over-ranks timing and whole-job throughput -- run as two
+gloo ranks on the CPU."""
+from __future__ import annotations
+
+import os
+import socket
+
+import numpy as np
+import torch.multiprocessing as mp
+
+import bench
+from split_kv_attention_flash_gb300 import workloads as wl
+
+
+def test_flop_counts_of_the_workloads():
+    # 2 * Sq * Sk_visible * H * (D_QK + D_V) over visible (query, key) pairs
+    assert bench.flops_of(wl.TARGET_SHAPE) == 2 * 4096 * 42700 * 12 * 320
+    assert abs(bench.flops_of(wl.LONG_VARLEN) - 7.7856768e12) < 1e3
+    assert bench.flops_of(wl.TINY_CAUSAL) == 2 * 2 * (64 * 65 // 2) * 128
+    causal = bench.flops_of(wl.MASKED_F16)                      # keys <= min(q, 3000)
+    assert causal == 2 * 16 * 256 * (2048 * 2049 // 2)
+    prefix = bench.flops_of(wl.MASKED_F16.with_(mask=wl.MASK_PREFIX_CAUSAL, prefix_offset=2048))
+    vis = np.minimum(np.arange(2048) + 2048, 3000) + 1
+    assert prefix == 2 * 16 * 256 * int(vis.sum())
+    fully_masked = wl.MASKED_F16.with_(mask=wl.MASK_PREFIX_CAUSAL, prefix_offset=-256)
+    assert bench.flops_of(fully_masked) == 2 * 16 * 256 * sum(max(0, q - 256 + 1) for q in range(2048))
+
+
+def test_combine_bytes():
+    w = wl.TARGET_SHAPE
+    counts = np.full(w.total_q, 3, dtype=np.int32)
+    b = bench.combine_bytes(w, counts, with_lse=False)
+    assert b == w.H * w.total_q * (3 * (4 * 128 + 4) + 128 * 2) + 4 * w.total_q
+
+
+def test_pages_baseline_figure():
+    # the split-3 time printed for this shape (2.269 ms) as TFLOP/s
+    assert abs(bench.PAGES_SPLIT3_TFLOPS - 591.99) < 0.1
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, queue):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local = [1.0 + rank, 5.0 - 2 * rank]          # per-rank step and e2e times, ms
+        ms, e2e = bench.max_over_ranks(local)
+        dist.barrier()
+        queue.put((rank, ms, e2e, bench.whole_job_tflops(1e12, world, ms)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    queue = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, queue)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = sorted(queue.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, e2e, tflops in results:
+        assert ms == 2.0 and e2e == 5.0            # both ranks see the slowest rank
+        assert abs(tflops - 2 * 1e12 / 2e-3 / 1e12) < 1e-9
+
+
+def test_single_process_is_identity():
+    assert bench.max_over_ranks([3.0, 4.5]) == [3.0, 4.5]
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    class Args:
+        workload, steps, warmup, cpu_seconds, gpus = "tiny", 1, 3, 1.0, 2
+    assert bench.run_reference(Args, rank=1) is None
