@@ -11,7 +11,10 @@
 //   * The M block is two 128-row MMA tiles Q0, Q1, kept in shared memory for the
 //     whole CTA (TMA, 128-byte swizzle). Keys stream through in tiles of 128.
 //   * Warp 8 (one lane) is the TMA producer: Q once, then K(j) and V(j) into
-//     rings of shared-memory stages guarded by full / empty mbarriers.
+//     rings of shared-memory stages guarded by full / empty mbarriers. With a single
+//     V stage (D_QK = 192, where Q takes 96 KB) the stage is two 64-key halves with
+//     their own barriers: PV1(j) frees the first half after its first four MMAs, so
+//     V(j+1) starts arriving before PV1(j) has finished.
 //   * Warp 9 (one lane) issues the tcgen05 MMAs: S_t = Q_t K(j)^T into TMEM
 //     (128 f32 columns per tile), then O_t += P_t V(j) with P_t read from TMEM and
 //     V(j) from shared memory (MN-major operand). The order
@@ -69,9 +72,13 @@ template <int DQK, int DV> struct Cfg {
     static constexpr int kBarQ = 0;
     static constexpr int kBarKF = 1;
     static constexpr int kBarKE = kBarKF + kKStages;
-    static constexpr int kBarVF = kBarKE + kKStages;
-    static constexpr int kBarVE = kBarVF + kVStages;
-    static constexpr int kBarS = kBarVE + kVStages;
+    static constexpr bool kSplitV = kVStages == 1;          // V stage in two 64-key halves
+    static constexpr int kVParts = kSplitV ? 2 : 1;
+    static constexpr int kVPartBytes = kVBytes / kVParts;
+    static constexpr int kVPanelBytes = kVPartBytes / (DV / 64);  // one 64-column panel of a part
+    static constexpr int kBarVF = kBarKE + kKStages;       // [stage][part]
+    static constexpr int kBarVE = kBarVF + kVParts * kVStages;
+    static constexpr int kBarS = kBarVE + kVParts * kVStages;
     static constexpr int kBarP = kBarS + 2;
     static constexpr int kBarO = kBarP + 2;
     static constexpr int kBarDrain = kBarO + 2;
@@ -80,6 +87,7 @@ template <int DQK, int DV> struct Cfg {
     static constexpr int kSmemBytes = 1024 + kTileBytes + kNumBars * 8 + 16;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "head dims");
+    static_assert(kSplitV == (DQK == 192), "the V tensor map's box rows follow this rule");
 };
 
 // Wait of a whole warp: every lane polls, the warp leaves together.
@@ -141,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(C::kBarKF + i), 1);
             ptx::mbar_init(bar(C::kBarKE + i), 1);
         }
-        for (int i = 0; i < C::kVStages; ++i) {
+        for (int i = 0; i < C::kVParts * C::kVStages; ++i) {
             ptx::mbar_init(bar(C::kBarVF + i), 1);
             ptx::mbar_init(bar(C::kBarVE + i), 1);
         }
@@ -193,14 +201,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_4d(sK + ks * C::kKBytes + c * kChunkBytes, &tmK,
                                      bar(C::kBarKF + ks), c * 64, krow + j * kBN, h, cb);
                 issued_k = j + 1;
-                ok = ptx::mbar_wait_bounded(bar(C::kBarVE + vs), ((j / C::kVStages) & 1) ^ 1,
-                                            abort_flag, p.err, kErrProducer, kTimeoutNs);
+                for (int hf = 0; hf < C::kVParts && ok; ++hf) {
+                    const int vb = C::kVParts * vs + hf;
+                    ok = ptx::mbar_wait_bounded(bar(C::kBarVE + vb), ((j / C::kVStages) & 1) ^ 1,
+                                                abort_flag, p.err, kErrProducer, kTimeoutNs);
+                    if (!ok) break;
+                    ptx::mbar_arrive_expect_tx(bar(C::kBarVF + vb), C::kVPartBytes);
+                    for (int c = 0; c < DV / 64; ++c)
+                        ptx::tma_load_4d(sV + vs * C::kVBytes + hf * C::kVPartBytes + c * C::kVPanelBytes,
+                                         &tmV, bar(C::kBarVF + vb), c * 64,
+                                         krow + j * kBN + hf * (kBN / C::kVParts), h, cb);
+                    issued_v = C::kVParts * j + hf + 1;
+                }
                 if (!ok) break;
-                ptx::mbar_arrive_expect_tx(bar(C::kBarVF + vs), C::kVBytes);
-                for (int c = 0; c < DV / 64; ++c)
-                    ptx::tma_load_4d(sV + vs * C::kVBytes + c * kChunkBytes, &tmV,
-                                     bar(C::kBarVF + vs), c * 64, krow + j * kBN, h, cb);
-                issued_v = j + 1;
             }
             if (!ok) {
                 // drain: every load already issued must land before the CTA exits
@@ -212,10 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_wait_bounded(bar(C::kBarKF + i), (last / C::kKStages) & 1, no_abort,
                                            nullptr, 0, kTimeoutNs);
                 }
-                for (int i = 0; i < C::kVStages && i < issued_v; ++i) {
-                    const int last = i + ((issued_v - 1 - i) / C::kVStages) * C::kVStages;
-                    ptx::mbar_wait_bounded(bar(C::kBarVF + i), (last / C::kVStages) & 1, no_abort,
-                                           nullptr, 0, kTimeoutNs);
+                // V parts are issued in the order P j, P j + 1, ... (P = kVParts) into
+                // barrier (j % kVStages) * P + part
+                constexpr int kVB = C::kVParts * C::kVStages;
+                for (int i = 0; i < kVB && i < issued_v; ++i) {
+                    const int last = i + ((issued_v - 1 - i) / kVB) * kVB;
+                    ptx::mbar_wait_bounded(bar(C::kBarVF + i), ((last / C::kVParts) / C::kVStages) & 1,
+                                           no_abort, nullptr, 0, kTimeoutNs);
                 }
             }
         }
@@ -237,12 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tc_commit(bar(C::kBarS + t));
             };
-            auto issue_pv = [&](int t, int j) {
-                const uint32_t vbase = sV + (j % C::kVStages) * C::kVBytes;
+            // O_t (+)= P_t V(j) over one V part (all 128 keys, or one 64-key half); N = DV
+            // spans the part's 64-column panels, kVPanelBytes apart
+            auto issue_pv_part = [&](int t, int j, int hf) {
+                constexpr int kSteps = kBN / 16 / C::kVParts;
+                const uint32_t vbase = sV + (j % C::kVStages) * C::kVBytes + hf * C::kVPartBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    ptx::mma_ts(tO[t], tS[t] + kk * 8, ptx::smem_desc_sw128(vbase + kk * 2048, kChunkBytes, 1024),
-                                kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                for (int k4 = 0; k4 < kSteps; ++k4) {
+                    const int kk = hf * kSteps + k4;
+                    ptx::mma_ts(tO[t], tS[t] + kk * 8,
+                                ptx::smem_desc_sw128(vbase + k4 * 2048, C::kVPanelBytes, 1024), kIdescPV,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                }
             };
             bool ok = ptx::mbar_wait_bounded(bar(C::kBarQ), 0, abort_flag, p.err, kErrMma, kTimeoutNs) &&
                       ptx::mbar_wait_bounded(bar(C::kBarKF), 0, abort_flag, p.err, kErrMma, kTimeoutNs);
@@ -255,13 +277,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int vs = j % C::kVStages;
                 const int kn = (j + 1) % C::kKStages;
-                ok = ptx::mbar_wait_bounded(bar(C::kBarVF + vs), (j / C::kVStages) & 1, abort_flag,
-                                            p.err, kErrMma, kTimeoutNs) &&
-                     ptx::mbar_wait_bounded(bar(C::kBarP + 0), j & 1, abort_flag, p.err, kErrMma,
+                const uint32_t vpar = (j / C::kVStages) & 1;
+                ok = ptx::mbar_wait_bounded(bar(C::kBarP + 0), j & 1, abort_flag, p.err, kErrMma,
                                             kTimeoutNs);
+                for (int hf = 0; hf < C::kVParts && ok; ++hf) {
+                    ok = ptx::mbar_wait_bounded(bar(C::kBarVF + C::kVParts * vs + hf), vpar, abort_flag,
+                                                p.err, kErrMma, kTimeoutNs);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    issue_pv_part(0, j, hf);
+                }
                 if (!ok) break;
-                ptx::tc_fence_after();
-                issue_pv(0, j);
                 if (j + 1 < n_tiles) {
                     ok = ptx::mbar_wait_bounded(bar(C::kBarKF + kn), ((j + 1) / C::kKStages) & 1,
                                                 abort_flag, p.err, kErrMma, kTimeoutNs);
@@ -273,8 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             kTimeoutNs);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                issue_pv(1, j);
-                ptx::tc_commit(bar(C::kBarVE + vs));
+                for (int hf = 0; hf < C::kVParts; ++hf) {
+                    issue_pv_part(1, j, hf);
+                    ptx::tc_commit(bar(C::kBarVE + C::kVParts * vs + hf));  // this part of V(j) is free
+                }
                 if (j + 1 < n_tiles) {
                     issue_qk(1, j + 1);
                     ptx::tc_commit(bar(C::kBarKE + kn));
@@ -449,16 +477,16 @@ static EncodeTiledFn encode_fn() {
 }
 
 // [rows, H, D] (varlen: rows = total, one batch) or [B][rows][H][D] (dense), box of
-// 64 elements x 128 rows, 128-byte swizzle; out-of-range rows read as zero.
+// 64 elements x box_rows rows, 128-byte swizzle; out-of-range rows read as zero.
 static bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long long rows, int H,
-                     int B, bool dense) {
+                     int B, bool dense, unsigned box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc || rows <= 0 || t.sr <= 0 || t.sh <= 0) return false;
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)(dense ? B : 1)};
     cuuint64_t strides[3] = {(cuuint64_t)t.sr * 2, (cuuint64_t)t.sh * 2,
                              (cuuint64_t)(dense ? t.sb : rows * t.sr) * 2};
     if (dense && t.sb <= 0) return false;
-    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t box[4] = {64, box_rows, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(m, dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                      4, t.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -516,9 +544,9 @@ cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, 
     CUtensorMap mq, mk, mv;
     const long long qrows = dense ? p.max_sq : p.total_q;
     const long long krows = dense ? p.max_sk : p.total_k;
-    if (!make_map(&mq, q, dtype, p.d_qk, qrows, p.H, p.B, dense) ||
-        !make_map(&mk, k, dtype, p.d_qk, krows, p.H, p.B, dense) ||
-        !make_map(&mv, v, dtype, p.d_v, krows, p.H, p.B, dense))
+    if (!make_map(&mq, q, dtype, p.d_qk, qrows, p.H, p.B, dense, 128) ||
+        !make_map(&mk, k, dtype, p.d_qk, krows, p.H, p.B, dense, 128) ||
+        !make_map(&mv, v, dtype, p.d_v, krows, p.H, p.B, dense, p.d_qk == 192 ? 64 : 128))
         return cudaSuccess;  // not expressible as TMA maps: the caller falls back
     *launched = true;
 #define SK_TC_DIMS(T)                                                                              \
