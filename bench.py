@@ -208,6 +208,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     p = skv.params_for(w, dev)
     S = skv.sk_auto_split_kv(p)
     p.split_kv = S
+    p.fuse_combine = int(args.fuse_combine)
     out = torch.empty(w.total_q, w.H, w.d_v, dtype=q.dtype, device=dev)
     lse = None
     ws = torch.empty(max(skv.sk_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
@@ -218,7 +219,8 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     def step():
         skv.sk_attn_fwd(p, q, k, v, out, lse, ws)
 
-    launches_per_step = 1 if S == 1 else 3
+    fused = bool(p.fuse_combine) and kname == "partial_tc" and S <= 8
+    launches_per_step = 1 if S == 1 or fused else 3   # counts, partial, combine
     sampler = ClockSampler(dev.index)
     with sampler:
         for _ in range(args.warmup):
@@ -309,7 +311,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "sequences": w.B, "seq_len_q": list(w.seqlens_q),
                    "seq_len_k": list(w.seqlens_k), "heads": w.H, "d_qk": w.d_qk, "d_v": w.d_v,
-                   "split_kv": S, "n_per_block": w.n_per_block,
+                   "split_kv": S, "n_per_block": w.n_per_block, "fuse_combine": p.fuse_combine,
                    "block_m": skv.sk_default_block_m(w.d_qk, w.d_v),
                    "flop_per_step": fl, "l2": "inputs larger than L2 "
                    f"({(q.numel() + k.numel() + v.numel()) * q.element_size() / 1e6:.0f} MB)",
@@ -371,6 +373,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(wl.ALL), default="target")
     ap.add_argument("--split", type=int, default=None, help="force split_kv (default: auto)")
+    ap.add_argument("--fuse-combine", action="store_true",
+                    help="merge the splits inside the tensor-core kernel (sk_params.fuse_combine)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -94,6 +94,10 @@ typedef struct {
     int split_kv;                /* 0: automatic (sk_auto_split_kv); else 1..32 */
     int block_m;                 /* query rows per M block of the partition; 0: default */
     float softmax_scale;         /* 0: 1/sqrt(d_qk) */
+    int fuse_combine;            /* sk_attn_fwd only, 0 or 1: 1 lets the tensor-core partial
+                                    kernel merge the splits itself (the last CTA of each M
+                                    block), instead of the separate combine; 0 (default)
+                                    keeps the combine kernel, which measured faster */
 } sk_params;
 
 /* Largest split_kv accepted. */

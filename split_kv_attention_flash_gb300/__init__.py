@@ -52,7 +52,7 @@ class _Params(ctypes.Structure):
                 ("mask", ctypes.c_int), ("prefix_offset", ctypes.c_int),
                 ("last_valid_kv_index", ctypes.c_int), ("n_per_block", ctypes.c_int),
                 ("split_kv", ctypes.c_int), ("block_m", ctypes.c_int),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("fuse_combine", ctypes.c_int)]
 
 
 class _Tensor(ctypes.Structure):
@@ -120,6 +120,7 @@ class Params:
     split_kv: int = 0
     block_m: int = 0
     softmax_scale: float = 0.0
+    fuse_combine: int = 0
 
     def c(self) -> _Params:
         def ptr(t):
@@ -132,7 +133,7 @@ class Params:
                        self.total_k, self.d_qk, self.d_v, ptr(self.cu_seqlens_q),
                        ptr(self.cu_seqlens_k), self.mask, self.prefix_offset,
                        self.last_valid_kv_index, self.n_per_block, self.split_kv, self.block_m,
-                       self.softmax_scale)
+                       self.softmax_scale, self.fuse_combine)
 
     @property
     def dense(self) -> bool:

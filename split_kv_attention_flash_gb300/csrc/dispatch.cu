@@ -20,8 +20,8 @@ cudaError_t run_partial(const Problem &p, int dtype, const TensorView &q, const 
                         float *lse_out, cudaStream_t st) {
     if (tc::partial_tc_supported(p, dtype)) {
         bool launched = false;
-        cudaError_t e = tc::launch_partial_tc(p, dtype, q, k, v, o_part, lse_part, out, lse_out, st,
-                                              &launched);
+        cudaError_t e = tc::launch_partial_tc(p, dtype, q, k, v, o_part, lse_part, out, lse_out,
+                                              nullptr, st, &launched);
         if (launched || e != cudaSuccess) return e;
     }
     if (dec::partial_decode_supported(p, dtype)) {
@@ -31,6 +31,16 @@ cudaError_t run_partial(const Problem &p, int dtype, const TensorView &q, const 
         if (launched || e != cudaSuccess) return e;
     }
     return launch_partial_simt(p, dtype, q, k, v, o_part, lse_part, out, lse_out, st);
+}
+
+cudaError_t run_partial_fused(const Problem &p, int dtype, const TensorView &q,
+                              const TensorView &k, const TensorView &v, float *o_part,
+                              float *lse_part, const TensorView &out, float *lse_out, int *tickets,
+                              cudaStream_t st, bool *fused) {
+    *fused = false;
+    if (!tc::partial_tc_supported(p, dtype)) return cudaSuccess;
+    return tc::launch_partial_tc(p, dtype, q, k, v, o_part, lse_part, &out, lse_out, tickets, st,
+                                 fused);
 }
 
 }  // namespace sk

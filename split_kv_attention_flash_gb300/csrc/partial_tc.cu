@@ -114,11 +114,112 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+constexpr int kMaxFusedSplits = 8;
+constexpr int kMergeBatch = 8;  // rows a warp loads at once
+constexpr int kMergePre = 3;    // splits per row among those loads (more are read afterwards)
+
+// Merge of one M block's splits, run by the 256 softmax threads of the CTA that finished
+// that (sequence, head, M block) last ([P1] NaN-safe merge over s < count, the count
+// being the per-row formula of the count kernel):
+//   1. thread i forms the weights of row pos0 + i: m = max(max_s L_s, lowest finite),
+//      w_s = exp(L_s - m), 1 / max(sum_s w_s, 1), and writes the row's LSE;
+//   2. warp w merges rows pos0 + 32 w .. + 31, eight rows at a time: every lane first
+//      issues the 16-byte loads of eight rows x three splits (partials written by this
+//      kernel, read through L2), then weights, sums and stores.
+template <typename T, int DV>
+__device__ __forceinline__ void merge_block(const Problem &p, const SeqInfo &si, int b, int h,
+                                            int pos0, const float *o_part, const float *lse_part,
+                                            const TensorView &out, float *lse_out, float *sW,
+                                            float *sInv, int *sCnt) {
+    constexpr int kLanes = DV / 4;
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = p.S;
+    const int64_t plane = p.total_q;
+    {
+        const int own = pos0 + tid;
+        int c = 0;
+        if (own < si.sq) {
+            c = valid_split_count(p, si.last_valid, own);
+            c = c < 1 ? 1 : (c > S ? S : c);
+        }
+        const float *lrow = lse_part + (int64_t)h * S * plane + si.q0 + own;
+        float l[kMaxFusedSplits];
+        float m = -FLT_MAX;
+#pragma unroll
+        for (int sp = 0; sp < kMaxFusedSplits; ++sp) {
+            l[sp] = sp < c ? __ldcg(lrow + sp * plane) : -INFINITY;
+            m = fmaxf(m, l[sp]);
+        }
+        float wsum = 0.f;
+#pragma unroll
+        for (int sp = 0; sp < kMaxFusedSplits; ++sp) {
+            const float w = sp < c ? expf(l[sp] - m) : 0.f;
+            sW[sp * 256 + tid] = w;
+            wsum += w;
+        }
+        sInv[tid] = 1.f / fmaxf(wsum, 1.f);
+        sCnt[tid] = c;
+        if (own < si.sq && lse_out)
+            lse_out[(int64_t)h * plane + si.q0 + own] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    const float *obase = o_part + ((int64_t)h * S * plane + si.q0 + pos0) * DV + lane * 4;
+    for (int r0 = 0; r0 < 32; r0 += kMergeBatch) {
+        const int rb = warp * 32 + r0;
+        if (pos0 + rb >= si.sq) break;  // warp-uniform
+        float4 o[kMergeBatch][kMergePre];
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const int ci = sCnt[rb + i];
+#pragma unroll
+            for (int sp = 0; sp < kMergePre; ++sp)
+                o[i][sp] = (sp < ci && lane < kLanes)
+                               ? __ldcg((const float4 *)(obase + ((int64_t)sp * plane + rb + i) * DV))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const int rl = rb + i;
+            if (pos0 + rl >= si.sq) break;  // warp-uniform
+            const int ci = sCnt[rl];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int sp = 0; sp < kMergePre; ++sp) {
+                const float w = sp < ci ? sW[sp * 256 + rl] : 0.f;
+                acc.x = fmaf(w, o[i][sp].x, acc.x);
+                acc.y = fmaf(w, o[i][sp].y, acc.y);
+                acc.z = fmaf(w, o[i][sp].z, acc.z);
+                acc.w = fmaf(w, o[i][sp].w, acc.w);
+            }
+            for (int sp = kMergePre; sp < ci; ++sp) {
+                const float4 v = lane < kLanes
+                                     ? __ldcg((const float4 *)(obase + ((int64_t)sp * plane + rl) * DV))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float w = sW[sp * 256 + rl];
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
+            const float inv = sInv[rl];
+            if (lane < kLanes) {
+                T *dst = (T *)out.ptr + row_offset(p, out, b, si.q0, pos0 + rl) + (int64_t)h * out.sh +
+                         lane * 4;
+                uint2 v;
+                v.x = ptx::pack2(acc.x * inv, acc.y * inv, kBF16);
+                v.y = ptx::pack2(acc.z * inv, acc.w * inv, kBF16);
+                *(uint2 *)dst = v;
+            }
+        }
+    }
+}
+
 template <typename T, int DQK, int DV, bool DIRECT>
 __global__ void __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, Problem p, float *o_part,
-                      float *lse_part, TensorView out, float *lse_out) {
+                      float *lse_part, TensorView out, float *lse_out, int *tickets) {
     using C = Cfg<DQK, DV>;
     constexpr bool kBF16 = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
@@ -141,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *const gen_base = smem_raw + (sQ - raw_u32);
     uint32_t *const tmem_holder = (uint32_t *)(gen_base + (bar0 - sQ) + C::kNumBars * 8);
     volatile int *const abort_flag = (volatile int *)(tmem_holder + 1);
+    volatile int *const fused_last = (volatile int *)(tmem_holder + 2);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
     if (threadIdx.x == 0) {
@@ -442,6 +544,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if constexpr (!DIRECT) {
+            // Fused merge: the CTA of this (sequence, head, M block) that writes its
+            // partials last merges all splits. Every softmax thread takes part in both
+            // barriers, also after an abort. Shared memory is free by now: every MMA and
+            // load of this CTA has completed.
+            if (tickets) {
+                __threadfence();
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (threadIdx.x == 0) {
+                    const int group = (b * p.H + h) * (int)gridDim.x + mb;
+                    *fused_last = !*abort_flag && atomicAdd(tickets + group, 1) == p.S - 1;
+                }
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                if (*fused_last) {
+                    __threadfence();
+                    float *sW = (float *)gen_base;  // [kMaxFusedSplits][256]
+                    merge_block<T, DV>(p, si, b, h, pos0, o_part, lse_part, out, lse_out, sW,
+                                       sW + kMaxFusedSplits * 256, (int *)(sW + (kMaxFusedSplits + 1) * 256));
+                }
+            }
+        }
     }
 
     ptx::tc_fence_before();
@@ -498,7 +621,7 @@ static bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long
 template <typename T, int DQK, int DV, bool DIRECT>
 static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                               const CUtensorMap &mv, float *o_part, float *lse_part,
-                              const TensorView &out, float *lse_out, cudaStream_t st) {
+                              const TensorView &out, float *lse_out, int *tickets, cudaStream_t st) {
     using C = Cfg<DQK, DV>;
     auto kern = partial_tc_kernel<T, DQK, DV, DIRECT>;
     static std::once_flag once[64];
@@ -511,16 +634,20 @@ static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mq, const CUt
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     dim3 grid((unsigned)((p.max_sq + kBM - 1) / kBM), (unsigned)p.H, (unsigned)(p.B * p.S));
-    kern<<<grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p, o_part, lse_part, out, lse_out);
+    kern<<<grid, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, p, o_part, lse_part, out, lse_out, tickets);
     return cudaGetLastError();
 }
 
+// out without tickets: S == 1, the kernel writes the output directly. out with
+// tickets: partials, merged by the last CTA of each M block. No out: partials only.
 template <typename T, int DQK, int DV>
 static cudaError_t launch_dims(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                const CUtensorMap &mv, float *o_part, float *lse_part,
-                               const TensorView *out, float *lse_out, cudaStream_t st) {
-    if (out) return launch_cfg<T, DQK, DV, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out, st);
-    return launch_cfg<T, DQK, DV, false>(p, mq, mk, mv, o_part, lse_part, TensorView{}, nullptr, st);
+                               const TensorView *out, float *lse_out, int *tickets, cudaStream_t st) {
+    if (out && !tickets)
+        return launch_cfg<T, DQK, DV, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out, nullptr, st);
+    return launch_cfg<T, DQK, DV, false>(p, mq, mk, mv, o_part, lse_part, out ? *out : TensorView{},
+                                         out ? lse_out : nullptr, out ? tickets : nullptr, st);
 }
 
 bool partial_tc_supported(const Problem &p, int dtype) {
@@ -537,9 +664,10 @@ bool partial_tc_supported(const Problem &p, int dtype) {
 
 cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, const TensorView &k,
                               const TensorView &v, float *o_part, float *lse_part,
-                              const TensorView *out, float *lse_out, cudaStream_t st,
+                              const TensorView *out, float *lse_out, int *tickets, cudaStream_t st,
                               bool *launched) {
     *launched = false;
+    if (tickets && (p.S < 2 || p.S > kMaxFusedSplits)) return cudaSuccess;  // not fusable
     const bool dense = p.cu_q == nullptr;
     CUtensorMap mq, mk, mv;
     const long long qrows = dense ? p.max_sq : p.total_q;
@@ -550,9 +678,9 @@ cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, 
         return cudaSuccess;  // not expressible as TMA maps: the caller falls back
     *launched = true;
 #define SK_TC_DIMS(T)                                                                              \
-    if (p.d_qk == 192) return launch_dims<T, 192, 128>(p, mq, mk, mv, o_part, lse_part, out, lse_out, st); \
-    if (p.d_qk == 128) return launch_dims<T, 128, 128>(p, mq, mk, mv, o_part, lse_part, out, lse_out, st); \
-    return launch_dims<T, 64, 64>(p, mq, mk, mv, o_part, lse_part, out, lse_out, st);
+    if (p.d_qk == 192) return launch_dims<T, 192, 128>(p, mq, mk, mv, o_part, lse_part, out, lse_out, tickets, st); \
+    if (p.d_qk == 128) return launch_dims<T, 128, 128>(p, mq, mk, mv, o_part, lse_part, out, lse_out, tickets, st); \
+    return launch_dims<T, 64, 64>(p, mq, mk, mv, o_part, lse_part, out, lse_out, tickets, st);
     if (dtype == kBF16) { SK_TC_DIMS(__nv_bfloat16) }
     SK_TC_DIMS(__half)
 #undef SK_TC_DIMS

@@ -55,6 +55,7 @@ sk_status check_params(const sk_params *p) {
     if (p->block_m < 0) return SK_ERR_INVALID_ARG;
     if (!(p->softmax_scale == p->softmax_scale) || isinf(p->softmax_scale))
         return SK_ERR_INVALID_ARG;
+    if (p->fuse_combine != 0 && p->fuse_combine != 1) return SK_ERR_INVALID_ARG;
     if (!sk_supported_head_dims(p->d_qk, p->d_v)) return SK_ERR_UNSUPPORTED;
     return SK_OK;
 }
@@ -127,9 +128,11 @@ sk_status cuda_status(cudaError_t e) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WorkspaceLayout {
-    size_t counts, o_part, lse_part, total;
+    size_t counts, o_part, lse_part, tickets, ticket_bytes, total;
 };
 
+// counts | O_part | L_part | tickets (one int per (sequence, head, 256-row M block), for
+// the merge fused into the tensor-core kernel), each 256-byte aligned
 WorkspaceLayout layout_for(const sk_params *p, int S) {
     WorkspaceLayout w{};
     if (S <= 1) return w;
@@ -137,7 +140,9 @@ WorkspaceLayout layout_for(const sk_params *p, int S) {
     w.counts = 0;
     w.o_part = align256(rows * 4);
     w.lse_part = w.o_part + align256((size_t)p->H * S * rows * p->d_v * 4);
-    w.total = w.lse_part + align256((size_t)p->H * S * rows * 4);
+    w.tickets = w.lse_part + align256((size_t)p->H * S * rows * 4);
+    w.ticket_bytes = (size_t)p->B * p->H * (((size_t)p->max_seqlen_q + 255) / 256) * 4;
+    w.total = w.tickets + align256(w.ticket_bytes);
     return w;
 }
 
@@ -284,6 +289,16 @@ sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
     int32_t *counts = (int32_t *)(ws + w.counts);
     float *o_part = (float *)(ws + w.o_part);
     float *lse_part = (float *)(ws + w.lse_part);
+    if (p->fuse_combine && pr.bm == 256) {
+        // the tensor-core kernel merges in its last CTA per M block: zeroed tickets, one launch
+        int *tickets = (int *)(ws + w.tickets);
+        cudaError_t e = cudaMemsetAsync(tickets, 0, w.ticket_bytes, cs);
+        bool fused = false;
+        if (e == cudaSuccess)
+            e = sk::run_partial_fused(pr, q.dtype, view(q), view(k), view(v), o_part, lse_part, ov,
+                                      lse_out, tickets, cs, &fused);
+        if (e != cudaSuccess || fused) return cuda_status(e);
+    }
     cudaError_t e = sk::launch_counts(pr, counts, cs);
     if (e == cudaSuccess)
         e = sk::run_partial(pr, q.dtype, view(q), view(k), view(v), o_part, lse_part, nullptr,

@@ -171,7 +171,7 @@ namespace tc {
 bool partial_tc_supported(const Problem &p, int dtype);
 cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, const TensorView &k,
                               const TensorView &v, float *o_part, float *lse_part,
-                              const TensorView *out, float *lse_out, cudaStream_t st,
+                              const TensorView *out, float *lse_out, int *tickets, cudaStream_t st,
                               bool *launched);
 }  // namespace tc
 namespace dec {

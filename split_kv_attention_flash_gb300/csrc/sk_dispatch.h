@@ -11,6 +11,16 @@ cudaError_t run_partial(const Problem &p, int dtype, const TensorView &q, const 
                         const TensorView &v, float *o_part, float *lse_part, const TensorView *out,
                         float *lse_out, cudaStream_t st);
 
+// The tensor-core partial kernel with the merge fused in: the last CTA of every
+// (sequence, head, M block) merges its splits into out / lse_out. `tickets` (one int per
+// (sequence, head, M block), zeroed beforehand) count the finished splits. Sets *fused
+// when it launched; otherwise nothing ran and the caller takes the counts / partial /
+// combine path.
+cudaError_t run_partial_fused(const Problem &p, int dtype, const TensorView &q,
+                              const TensorView &k, const TensorView &v, float *o_part,
+                              float *lse_part, const TensorView &out, float *lse_out, int *tickets,
+                              cudaStream_t st, bool *fused);
+
 // Name of the kernel run_partial would launch.
 const char *partial_kernel_name(const Problem &p, int dtype, const TensorView &q,
                                 const TensorView &k, const TensorView &v);

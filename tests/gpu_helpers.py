@@ -31,8 +31,8 @@ def resolved_split(w, dev) -> int:
     return skv.sk_auto_split_kv(skv.params_for(w, dev))
 
 
-def run_fwd(w, qd, kd, vd, dev, split_kv=None, with_lse=True):
-    p = skv.params_for(w, dev, split_kv=split_kv)
+def run_fwd(w, qd, kd, vd, dev, split_kv=None, with_lse=True, fuse_combine=0):
+    p = skv.params_for(w, dev, split_kv=split_kv, fuse_combine=fuse_combine)
     out = torch.empty(w.total_q, w.H, w.d_v, dtype=qd.dtype, device=dev)
     lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=dev) if with_lse else None
     nbytes = skv.sk_workspace_bytes(p)

@@ -75,6 +75,7 @@ def _fwd(L, p, q=None, k=None, v=None, out=None, ws=FAKE, ws_bytes=1 << 40):
     (dict(split_kv=-1), SK_ERR_INVALID_ARG),
     (dict(block_m=-4), SK_ERR_INVALID_ARG),
     (dict(softmax_scale=float("nan")), SK_ERR_INVALID_ARG),
+    (dict(fuse_combine=2), SK_ERR_INVALID_ARG),
     (dict(d_qk=96, d_v=96), SK_ERR_UNSUPPORTED),
     (dict(d_qk=128, d_v=64), SK_ERR_UNSUPPORTED),
 ])
@@ -106,7 +107,9 @@ def test_workspace_layout_sizes(L):
         return (x + 255) // 256 * 256
     for S, tq, H, dv in ((3, 100, 4, 128), (8, 16384, 12, 128), (2, 1, 1, 64)):
         p = _params(split_kv=S, total_q=tq, H=H, d_qk=dv, d_v=dv)
-        assert skv.sk_workspace_bytes(p) == a256(4 * tq) + a256(4 * H * S * tq * dv) + a256(4 * H * S * tq)
+        tickets = p.B * H * ((p.max_seqlen_q + 255) // 256) * 4
+        assert skv.sk_workspace_bytes(p) == (a256(4 * tq) + a256(4 * H * S * tq * dv)
+                                            + a256(4 * H * S * tq) + a256(tickets))
     assert skv.sk_workspace_bytes(_params(split_kv=1)) == 0
 
 

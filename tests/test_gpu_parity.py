@@ -272,3 +272,27 @@ def test_config_long_varlen_full():
 def test_config_decode_full():
     w = wl.DECODE
     _sampled_check(w, [0, 1, 2, 4, 8, 16, 32], seq_subset=[0, 7, 19, 31])
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[2], SMALL[4], SMALL[-1]], ids=lambda w: w.name)
+def test_fused_merge_matches_separate_combine(w):
+    """sk_attn_fwd with fuse_combine = 1 (the tensor-core kernel merges in the last CTA of
+    each M block) against the default one-call path and the three separate calls."""
+    (_, _, _), (qd, kd, vd) = _inputs(w)
+    S = H.resolved_split(w, DEV)
+    out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV, split_kv=S, fuse_combine=1)
+    ref, ref_lse, _ = H.run_fwd(w, qd, kd, vd, DEV, split_kv=S)
+    o_part, l_part, p = H.run_partials(w, qd, kd, vd, DEV, S)
+    counts = torch.empty(w.total_q, dtype=torch.int32, device=DEV)
+    skv.sk_valid_split_counts(p, counts)
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    skv.sk_combine(p, o_part, l_part, counts, out2, lse2)
+    torch.cuda.synchronize()
+    for o, l in ((out2, lse2), (ref, ref_lse)):
+        assert (out.float() - o.float()).abs().max().item() <= H.TOL_O[w.dtype]
+        inf = torch.isneginf(l)
+        assert torch.equal(torch.isneginf(lse), inf)
+        assert (lse[~inf] - l[~inf]).abs().max().item() <= 1e-5
+    # a second call reuses the workspace: every call zeroes the tickets
+    out3, lse3, _ = H.run_fwd(w, qd, kd, vd, DEV, split_kv=S, fuse_combine=1)
+    assert torch.equal(out, out3) and torch.equal(lse, lse3)
