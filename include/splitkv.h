@@ -132,8 +132,10 @@ sk_status sk_attn_partial_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_t
 
 /*
  * sk_combine -- [P1] Technical details, NaN-safe merge (computeFinalAttentionStage)
- * and f32 merge for f16/bf16. Per (head, row), over the splits s < counts[row] only
- * (the others are never read):
+ * and f32 merge for f16/bf16. Per (head, row), over the splits s < counts[row] that the
+ * partition of the row's M block leaves non-empty (the others are never read: [P1]
+ * review notes allow a split with nothing to do to write nothing; such a split would
+ * contribute exactly 0):
  *   m = max(max_s L_s, lowest finite f32);  w_s = exp(L_s - m)
  *   O = sum_s w_s O_s / max(sum_s w_s, 1)   (in f32, then cast to out.dtype)
  *   lse_out = m + log(sum_s w_s), or -inf when that sum is 0
@@ -146,7 +148,8 @@ sk_status sk_combine(const sk_params *p, const float *o_part, const float *lse_p
 /*
  * sk_attn_fwd -- the whole forward pass in one call: counts, partials, combine.
  * With S == 1 the partial kernel writes `out` and `lse_out` directly and no
- * workspace is used. Otherwise `workspace` (device, 256-byte aligned, at least
+ * workspace is used. With S > 1, splits that hold no key of their M block write
+ * nothing (a real early exit) and the merge skips them. Otherwise `workspace` (device, 256-byte aligned, at least
  * sk_workspace_bytes()) holds the counts and the partials. max_seqlen_k == 0 writes
  * O = 0 and LSE = -inf ([P2] review: forced split with empty K must not raise;
  * [P1]: an empty split's LSE is -inf). lse_out may be NULL.

@@ -1,7 +1,8 @@
 // combine.cu -- NaN-safe f32 merge of split partials ([P1] Technical details:
 // NaN-safe merge (computeFinalAttentionStage), f32 merge for f16/bf16).
 //
-// Per (head, row), over the splits s < count (the others are never read):
+// Per (head, row), over the splits s < count that the row's block partition leaves
+// non-empty (the others are never read; an empty split contributes exactly 0):
 //   m = max(max_s L_s, lowest finite);  w_s = exp(L_s - m)
 //   O = sum_s w_s O_s / max(sum_s w_s, 1);   LSE = m + log(sum_s w_s)  (or -inf)
 //
@@ -66,9 +67,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
         const int r = warp * kRowsPerWarp + i;
-        int c = r < nrows ? __ldg(counts + row0 + r) : 0;
-        cnt[i] = c < 0 ? 0 : (c > S ? S : c);
-        if (r < nrows && cnt[i] < 1) cnt[i] = 1;
+        cnt[i] = r < nrows ? merged_splits(p, si.sq, si.last_valid, pos0 + r, __ldg(counts + row0 + r)) : 0;
     }
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -83,11 +82,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     // ---- weights: warp 0, one lane per row
     if (warp == 0) {
         const int r = lane;
-        int c = 0;
-        if (r < nrows) {
-            c = __ldg(counts + row0 + r);
-            c = c < 1 ? 1 : (c > S ? S : c);
-        }
+        const int c = r < nrows ? merged_splits(p, si.sq, si.last_valid, pos0 + r, __ldg(counts + row0 + r)) : 0;
         const float *lrow = lse_part + (int64_t)h * S * plane + row0 + r;
         float m = -FLT_MAX;  // max(max_s L_s, lowest finite)
         for (int s = 0; s < c; ++s) {
@@ -184,11 +179,9 @@ __global__ void __launch_bounds__(kBulkThreads)
     const float *sO = (const float *)sO_raw;
 
     if (warp == 0) {
-        int c = 0;
-        if (lane < nrows) {
-            c = __ldg(counts + row0 + lane);
-            c = c < 1 ? 1 : (c > S ? S : c);
-        }
+        const int c = lane < nrows
+                          ? merged_splits(p, si.sq, si.last_valid, pos0 + lane, __ldg(counts + row0 + lane))
+                          : 0;
         sCnt[lane] = c;
         int cmax = c;
 #pragma unroll

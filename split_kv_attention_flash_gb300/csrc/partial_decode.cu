@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kThreads, NR <= 4 ? 2 : 1)
     int kb, ke;
     split_key_range(p, si.sq, si.last_valid, 0, s, kb, ke);
     const int n_tiles = ke > kb ? (ke - kb + kKT - 1) / kKT : 0;
+    if (!DIRECT && n_tiles == 0 && p.skip_empty) return;  // real early exit: nothing is read
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);

@@ -72,6 +72,17 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
     const int t_begin = sRange[0], t_end = sRange[1];
+    // real early exit: no row of this CTA has a key in the split (the merge never reads it)
+    if (!DIRECT && p.skip_empty && t_begin >= t_end) {
+        bool all_empty = true;
+        for (int rr = 0; rr < kRows && all_empty; ++rr) {
+            if (pos0 + rr >= si.sq) break;
+            int rkb, rke;
+            split_key_range(p, si.sq, si.last_valid, pos0 + rr, s, rkb, rke);
+            all_empty = rke <= rkb;
+        }
+        if (all_empty) return;
+    }
 
     float m = -INFINITY;    // running max, base-2 scaled scores
     float l = 0.f;          // this thread's share of the running sum

@@ -139,10 +139,7 @@ __device__ __forceinline__ void merge_block(const Problem &p, const SeqInfo &si,
     {
         const int own = pos0 + tid;
         int c = 0;
-        if (own < si.sq) {
-            c = valid_split_count(p, si.last_valid, own);
-            c = c < 1 ? 1 : (c > S ? S : c);
-        }
+        if (own < si.sq) c = merged_splits(p, si.sq, si.last_valid, own, valid_split_count(p, si.last_valid, own));
         const float *lrow = lse_part + (int64_t)h * S * plane + si.q0 + own;
         float l[kMaxFusedSplits];
         float m = -FLT_MAX;
@@ -232,6 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kb, ke;
     split_key_range(p, si.sq, si.last_valid, pos0, s, kb, ke);
     const int n_tiles = ke > kb ? (ke - kb + kBN - 1) / kBN : 0;
+    // real early exit: a split without keys writes nothing (the merge never reads it)
+    if (!DIRECT && n_tiles == 0 && p.skip_empty && tickets == nullptr) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);

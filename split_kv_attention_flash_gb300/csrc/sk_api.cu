@@ -300,8 +300,10 @@ sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
         if (e != cudaSuccess || fused) return cuda_status(e);
     }
     cudaError_t e = sk::launch_counts(pr, counts, cs);
+    sk::Problem pe = pr;
+    pe.skip_empty = 1;  // splits without keys write nothing; the combine never reads them
     if (e == cudaSuccess)
-        e = sk::run_partial(pr, q.dtype, view(q), view(k), view(v), o_part, lse_part, nullptr,
+        e = sk::run_partial(pe, q.dtype, view(q), view(k), view(v), o_part, lse_part, nullptr,
                             nullptr, cs);
     if (e == cudaSuccess) e = sk::launch_combine(pr, out.dtype, o_part, lse_part, counts, ov, lse_out, cs);
     return cuda_status(e);

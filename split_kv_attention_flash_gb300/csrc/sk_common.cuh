@@ -28,6 +28,7 @@ struct Problem {
     float scale;                 // softmax scale
     float scale_log2;            // scale * log2(e): scores are kept in base 2
     int *err;                    // device error word (bounded waits), may be null
+    int skip_empty;              // 1: split CTAs with no key exit without writing (sk_attn_fwd)
 };
 
 // A [rows, heads, dim] view with element strides (dense layout adds stride_b).
@@ -119,6 +120,28 @@ __host__ __device__ inline void split_key_range(const Problem &p, int sq, int la
     kb = (int)(t0 * p.bn);
     long long e = t1 * p.bn;
     ke = (int)(e < bl + 1 ? e : bl + 1);
+}
+
+// Splits that the partition of the M block holding query `pos` leaves non-empty: the
+// first ceil(tiles / itersPerBlock) of them. The merge never reads the others ([P1]
+// review notes on a real early exit: a split with nothing to do may write nothing,
+// so the merge must not assume its memory was written).
+__host__ __device__ inline int nonempty_splits(const Problem &p, int sq, int last_valid, int pos) {
+    long long first = (long long)(pos / p.bm) * p.bm;
+    long long last_row = first + p.bm - 1;
+    if (last_row > sq - 1) last_row = sq - 1;
+    long long bl = covered_last(p, last_valid, last_row);
+    if (bl < 0) return 0;
+    long long nt = (bl + p.bn) / p.bn;
+    long long it = (nt + p.S - 1) / p.S;
+    return (int)((nt + it - 1) / it);
+}
+
+// Splits the merge reads for query `pos`: min(count, non-empty splits of its block).
+__device__ inline int merged_splits(const Problem &p, int sq, int last_valid, int pos, int count) {
+    int c = count < 1 ? 1 : (count > p.S ? p.S : count);
+    const int ne = nonempty_splits(p, sq, last_valid, pos);
+    return c < ne ? c : ne;
 }
 
 // Last key query `pos` may see, ignoring the split: lastValid, and q + offset

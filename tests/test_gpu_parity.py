@@ -296,3 +296,26 @@ def test_fused_merge_matches_separate_combine(w):
     # a second call reuses the workspace: every call zeroes the tickets
     out3, lse3, _ = H.run_fwd(w, qd, kd, vd, DEV, split_kv=S, fuse_combine=1)
     assert torch.equal(out, out3) and torch.equal(lse, lse3)
+
+
+@pytest.mark.parametrize("w", [wl.TINY_CAUSAL, SMALL[3], SMALL[4]], ids=lambda w: w.name)
+def test_combine_never_reads_partition_empty_splits(w):
+    """Splits the M-block partition leaves empty may hold anything (sk_attn_fwd does not
+    write them): poisoning them with NaN changes nothing."""
+    (_, _, _), (qd, kd, vd) = _inputs(w)
+    S = H.resolved_split(w, DEV)
+    o_part, l_part, p = H.run_partials(w, qd, kd, vd, DEV, S)
+    counts = torch.empty(w.total_q, dtype=torch.int32, device=DEV)
+    skv.sk_valid_split_counts(p, counts)
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=qd.dtype, device=DEV)
+    lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=DEV)
+    skv.sk_combine(p, o_part, l_part, counts, out, lse)
+    kb, ke = oracle.split_ranges(H.oracle_problem(w, S))                 # [total_q, S]
+    empty = torch.from_numpy(ke <= kb).to(DEV).T                          # [S, total_q]
+    assert empty.any()
+    o_bad = o_part.masked_fill(empty[None, :, :, None], float("nan"))
+    l_bad = l_part.masked_fill(empty[None], float("nan"))
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    skv.sk_combine(p, o_bad, l_bad, counts, out2, lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
