@@ -53,7 +53,8 @@ class _Problem(ctypes.Structure):
                 ("cu_k", ctypes.POINTER(ctypes.c_int32)), ("mask", ctypes.c_int),
                 ("prefix_offset", ctypes.c_int), ("last_valid_kv_index", ctypes.c_int),
                 ("n_per_block", ctypes.c_int), ("split_kv", ctypes.c_int),
-                ("block_m", ctypes.c_int), ("scale", ctypes.c_double)]
+                ("block_m", ctypes.c_int), ("scale", ctypes.c_double),
+                ("window_left", ctypes.c_int), ("seqused_k", ctypes.POINTER(ctypes.c_int32))]
 
 
 class _Array(ctypes.Structure):
@@ -101,7 +102,8 @@ class Problem:
 
     cu_q / cu_k are the cumulative sequence lengths ([B+1], starting at 0);
     mask is MASK_NONE / MASK_CAUSAL / MASK_PREFIX_CAUSAL; last_valid_kv_index -1
-    means "each sequence's last key"; scale None means 1/sqrt(d_qk).
+    means "each sequence's last key"; scale None means 1/sqrt(d_qk); window_left -1 means
+    no sliding window; seqused_k (per sequence) shortens padded key slots.
     """
     cu_q: list
     cu_k: list
@@ -115,6 +117,8 @@ class Problem:
     split_kv: int = 1
     block_m: int = 256
     scale: float | None = None
+    window_left: int = -1
+    seqused_k: list | None = None
     _keep: list = field(default_factory=list, repr=False)
 
     @property
@@ -133,12 +137,18 @@ class Problem:
         cq = np.ascontiguousarray(np.asarray(self.cu_q, dtype=np.int32))
         ck = np.ascontiguousarray(np.asarray(self.cu_k, dtype=np.int32))
         self._keep = [cq, ck]
+        used = None
+        if self.seqused_k is not None:
+            su = np.ascontiguousarray(np.asarray(self.seqused_k, dtype=np.int32))
+            self._keep.append(su)
+            used = su.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
         scale = self.scale if self.scale is not None else 1.0 / float(np.sqrt(self.d_qk))
         return _Problem(self.B, self.H, self.d_qk, self.d_v,
                         cq.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                         ck.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                         self.mask, self.prefix_offset, self.last_valid_kv_index,
-                        self.n_per_block, self.split_kv, self.block_m, scale)
+                        self.n_per_block, self.split_kv, self.block_m, scale,
+                        self.window_left, used)
 
 
 def _as_array(x, keep: list) -> _Array:

@@ -68,6 +68,8 @@ int orc_check_problem(const orc_problem *p)
         return -1;
     if (p->last_valid_kv_index < -1)
         return -1;
+    if (p->window_left < -1 || (p->window_left >= 0 && p->mask == ORC_MASK_NONE))
+        return -1;
     for (int b = 0; b < p->B; ++b)
         if (p->cu_q[b + 1] < p->cu_q[b] || p->cu_k[b + 1] < p->cu_k[b])
             return -1;
@@ -75,7 +77,15 @@ int orc_check_problem(const orc_problem *p)
 }
 
 static int seq_len_q(const orc_problem *p, int b) { return p->cu_q[b + 1] - p->cu_q[b]; }
-static int seq_len_k(const orc_problem *p, int b) { return p->cu_k[b + 1] - p->cu_k[b]; }
+/* Keys of sequence b: its cu_seqlens slot, shortened to seqused_k[b] when the slot is
+ * padded ([P2] Technical details: padded cu_seqlens). */
+static int seq_len_k(const orc_problem *p, int b)
+{
+    int n = p->cu_k[b + 1] - p->cu_k[b];
+    if (p->seqused_k && p->seqused_k[b] < n)
+        n = p->seqused_k[b] < 0 ? 0 : p->seqused_k[b];
+    return n;
+}
 
 /* Query position offset added before the causal comparison: 0 for plain causal. */
 static int offset_of(const orc_problem *p)
@@ -93,14 +103,20 @@ int orc_last_valid(const orc_problem *p, int b)
     return last;
 }
 
-/* Key j is visible to query q when it is a valid key and, under a causal mask,
- * not after q + prefix_offset. */
+/* Key j is visible to query q when it is a valid key and, under a causal mask, not
+ * after q + prefix_offset; with a sliding window ([P2] Technical details: the forced
+ * split honours the caller's window) also not before q + prefix_offset - window_left. */
 int orc_visible(const orc_problem *p, int b, int q, int j)
 {
     if (j < 0 || j > orc_last_valid(p, b))
         return 0;
-    if (p->mask != ORC_MASK_NONE && (long long)j > (long long)q + offset_of(p))
-        return 0;
+    if (p->mask != ORC_MASK_NONE) {
+        long long diag = (long long)q + offset_of(p);
+        if ((long long)j > diag)
+            return 0;
+        if (p->window_left >= 0 && (long long)j < diag - p->window_left)
+            return 0;
+    }
     return 1;
 }
 

@@ -13,7 +13,8 @@
  *        merge for f16/bf16; review notes on the conservativeness argument.
  *   [P2] "[ASM] [HIP] [JIT] [gfx942] Optimize long-context FMHA with split-KV"
  *        (ROCm/aiter pull request 5592): Motivation (packed varlen, D_QK != D_V),
- *        Technical details (num_splits semantics).
+ *        Technical details (num_splits semantics; the forced split honours the
+ *        caller's causal mask, window and padded cu_seqlens).
  *
  * All arithmetic is in double precision, starting from the stored (rounded)
  * input values, which are converted to double exactly.
@@ -50,6 +51,10 @@ typedef struct {
     int split_kv;                 /* number of splits S (>= 1) */
     int block_m;                  /* query rows per M block of the kernel partition (> 0) */
     double scale;                 /* softmax scale applied to q.k */
+    int window_left;              /* -1: none; else (causal masks only) keys before
+                                     q + offset - window_left are not visible */
+    const int32_t *seqused_k;     /* NULL, or host int32 [B]: keys of sequence b at or past
+                                     seqused_k[b] are padding (not part of the sequence) */
 } orc_problem;
 
 typedef struct {

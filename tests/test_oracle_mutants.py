@@ -25,13 +25,17 @@ MUTANTS = [
     ("partition uses the block's first row",
      "long long block_last = covered_last(p, b, last_row);",
      "long long block_last = covered_last(p, b, first_row);"),
-    ("causal comparison off by one", "(long long)j > (long long)q + offset_of(p)",
-     "(long long)j >= (long long)q + offset_of(p)"),
+    ("causal comparison off by one", "if ((long long)j > diag)", "if ((long long)j >= diag)"),
     ("prefix offset dropped", "return p->mask == ORC_MASK_PREFIX_CAUSAL ? p->prefix_offset : 0;",
      "return 0;"),
     ("last_valid_kv_index ignored", "if (p->last_valid_kv_index >= 0 && p->last_valid_kv_index < last)",
      "if (0)"),
     ("softmax scale dropped", "double sc = p->scale * dot;", "double sc = dot;"),
+    ("sliding window ignored", "if (p->window_left >= 0 && (long long)j < diag - p->window_left)",
+     "if (0)"),
+    ("sliding window off by one", "(long long)j < diag - p->window_left)",
+     "(long long)j <= diag - p->window_left)"),
+    ("padded key slots used in full", "if (p->seqused_k && p->seqused_k[b] < n)", "if (0)"),
     ("key read with the wrong head", "orc_load(K, (krow * H + h) * dqk + d)",
      "orc_load(K, (krow * H + 0) * dqk + d)"),
     ("keys summed in place of values", "o[d] += w * orc_load(V, (krow * H + h) * dv + d);",

@@ -34,29 +34,35 @@ MASKS = {"none": orc.MASK_NONE, "causal": orc.MASK_CAUSAL, "prefix_causal": orc.
 
 # ----------------------------------------------------------------- helpers
 
-def _visible_matrix(sq, sk, mask, po, lvi):
+def _visible_matrix(sq, sk, mask, po, lvi, window=-1, used=None):
     """Visibility straight from the page's wording: key j is valid when
     j <= lastValid (last_valid_kv_index, default seq_len_k - 1), and under a
-    causal / prefix-causal mask also j <= q + prefix_offset."""
-    last = sk - 1 if lvi < 0 else min(lvi, sk - 1)
+    causal / prefix-causal mask also j <= q + prefix_offset; a sliding window keeps
+    j >= q + offset - window; keys at or past `used` are padding."""
+    n = sk if used is None else min(sk, max(used, 0))
+    last = n - 1 if lvi < 0 else min(lvi, n - 1)
     q = np.arange(sq)[:, None]
     j = np.arange(sk)[None, :]
     vis = j <= last
     if mask != orc.MASK_NONE:
         off = po if mask == orc.MASK_PREFIX_CAUSAL else 0
         vis = vis & (j <= q + off)
+        if window >= 0:
+            vis = vis & (j >= q + off - window)
     return np.broadcast_to(vis, (sq, sk)).copy()
 
 
 def _random_problem(rng, B, H, dqk, dv, mask, po=0, lvi=-1, bn=16, S=3, bm=16,
-                    sq_max=24, sk_max=70, allow_empty=True):
+                    sq_max=24, sk_max=70, allow_empty=True, window=-1, padded=False):
     lo = 0 if allow_empty else 1
     sq = [int(rng.integers(1, sq_max + 1)) for _ in range(B)]
     sk = [int(rng.integers(lo, sk_max + 1)) for _ in range(B)]
     cu_q = np.concatenate([[0], np.cumsum(sq)]).tolist()
     cu_k = np.concatenate([[0], np.cumsum(sk)]).tolist()
+    used = [int(rng.integers(0, n + 3)) for n in sk] if padded else None
     prob = orc.Problem(cu_q=cu_q, cu_k=cu_k, H=H, d_qk=dqk, d_v=dv, mask=mask, prefix_offset=po,
-                       last_valid_kv_index=lvi, n_per_block=bn, split_kv=S, block_m=bm)
+                       last_valid_kv_index=lvi, n_per_block=bn, split_kv=S, block_m=bm,
+                       window_left=window, seqused_k=used)
     g = torch.Generator().manual_seed(int(rng.integers(1 << 30)))
     q = torch.randn(cu_q[-1], H, dqk, generator=g, dtype=torch.float64)
     k = torch.randn(cu_k[-1], H, dqk, generator=g, dtype=torch.float64)
@@ -73,7 +79,9 @@ def _library_attention(prob, q, k, v, key_range=None):
         q0, q1 = prob.cu_q[b], prob.cu_q[b + 1]
         k0, k1 = prob.cu_k[b], prob.cu_k[b + 1]
         sq, sk = q1 - q0, k1 - k0
-        vis = _visible_matrix(sq, sk, prob.mask, prob.prefix_offset, prob.last_valid_kv_index)
+        used = None if prob.seqused_k is None else prob.seqused_k[b]
+        vis = _visible_matrix(sq, sk, prob.mask, prob.prefix_offset, prob.last_valid_kv_index,
+                              prob.window_left, used)
         if key_range is not None:
             kb, ke = key_range(b)
             inr = np.zeros((sq, sk), dtype=bool)
@@ -137,12 +145,15 @@ def check_counts_bruteforce(n_configs=2500, seed=11):
         mask = int(rng.integers(0, 3))
         po = int(rng.integers(-sq - 2, sk + 3)) if mask == orc.MASK_PREFIX_CAUSAL else 0
         lvi = int(rng.choice([-1, -1, 0, 20, 1000]))
+        window = int(rng.choice([-1, -1, 0, 5, 40])) if mask != orc.MASK_NONE else -1
+        used = int(rng.integers(0, sk + 2)) if rng.random() < 0.3 else None
         p = orc.Problem(cu_q=[0, sq], cu_k=[0, sk], H=1, d_qk=4, d_v=4, mask=mask,
                         prefix_offset=po, last_valid_kv_index=lvi, n_per_block=bn, split_kv=S,
-                        block_m=bm)
+                        block_m=bm, window_left=window,
+                        seqused_k=None if used is None else [used])
         counts = orc.split_counts(p)
         kb, ke = orc.split_ranges(p)
-        vis = _visible_matrix(sq, sk, mask, po, lvi)
+        vis = _visible_matrix(sq, sk, mask, po, lvi, window, used)
         j = np.arange(sk)
         in_split = (j[None, None, :] >= kb[:, :, None]) & (j[None, None, :] < ke[:, :, None])
         holds = (in_split & vis[:, None, :]).any(axis=2)                 # [sq, S]
@@ -154,7 +165,7 @@ def check_counts_bruteforce(n_configs=2500, seed=11):
         needed = np.where(holds.any(axis=1), S - np.argmax(holds[:, ::-1], axis=1), 1)
         assert (counts >= 1).all() and (counts <= S).all()
         assert (counts >= needed).all(), (sq, sk, bn, S, bm, mask, po, lvi)
-        if bm == 1 and sk > 0:
+        if bm == 1 and sk > 0 and (used is None or used > 0):
             # one row per block: the kernel's partition is the row's own, so the
             # count is exactly the number of non-empty splits
             assert (counts == nonempty.sum(axis=1)).all()
@@ -169,6 +180,35 @@ def check_attention_vs_library(seed=5):
         out, lse = orc.attention(prob, q, k, v, nthreads=2)
         ref_o, ref_l, empty = _library_attention(prob, q, k, v)
         _compare_to_library(out, lse, ref_o, ref_l, empty)
+
+
+def check_window_and_padding_vs_library(seed=12):
+    """Sliding window ([P2]: the forced split honours the caller's window) and padded key
+    slots with a per-sequence used count ([P2]: padded cu_seqlens): unsplit attention
+    and every split's partial against the library routine, and merge == unsplit."""
+    rng = np.random.default_rng(seed)
+    for mask, po, window, padded in ((orc.MASK_CAUSAL, 0, 6, False),
+                                     (orc.MASK_PREFIX_CAUSAL, 25, 17, True),
+                                     (orc.MASK_PREFIX_CAUSAL, -4, 0, True),
+                                     (orc.MASK_NONE, 0, -1, True)):
+        prob, q, k, v = _random_problem(rng, B=3, H=2, dqk=16, dv=8, mask=mask, po=po, bn=8,
+                                        S=4, bm=8, window=window, padded=padded)
+        out, lse = orc.attention(prob, q, k, v, nthreads=2)
+        ref_o, ref_l, empty = _library_attention(prob, q, k, v)
+        _compare_to_library(out, lse, ref_o, ref_l, empty)
+        o_part, l_part = orc.partials(prob, q, k, v)
+        kb, ke = orc.split_ranges(prob)
+        for s_ in range(prob.split_kv):
+            def key_range(b, s_=s_):
+                r0, r1 = prob.cu_q[b], prob.cu_q[b + 1]
+                return kb[r0:r1, s_], ke[r0:r1, s_]
+            r_o, r_l, emp = _library_attention(prob, q, k, v, key_range=key_range)
+            _compare_to_library(o_part[:, :, s_], l_part[:, :, s_], r_o, r_l, emp)
+        out_m, lse_m = orc.merge(o_part, l_part, orc.split_counts(prob))
+        assert np.abs(out_m - out).max() < 1e-12
+        fin = np.isfinite(lse)
+        assert np.array_equal(np.isneginf(lse_m), ~fin)
+        assert np.abs(lse_m[fin] - lse[fin]).max(initial=0) < 1e-12
 
 
 def check_attention_closed_forms(seed=6):
@@ -297,6 +337,7 @@ def check_storage_widening():
 
 
 ALL_CHECKS = [check_worked_counts, check_counts_bruteforce, check_attention_vs_library,
+              check_window_and_padding_vs_library,
               check_attention_closed_forms, check_partials_vs_library, check_merge_equals_unsplit,
               check_merge_clamps, check_split_one_is_unsplit, check_storage_widening]
 
@@ -316,3 +357,5 @@ def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         orc.split_counts(orc.Problem(cu_q=[0, 4], cu_k=[0, 8], H=1, d_qk=4, d_v=4,
                                      last_valid_kv_index=-2))
+    with pytest.raises(ValueError):   # a window needs a causal mask
+        orc.split_counts(orc.Problem(cu_q=[0, 4], cu_k=[0, 8], H=1, d_qk=4, d_v=4, window_left=3))
