@@ -49,6 +49,8 @@ def flops_of(w, rows=None) -> float:
     total = 0
     for b in range(w.B):
         sq, sk = w.seqlens_q[b], w.seqlens_k[b]
+        if w.seqused_k is not None:
+            sk = min(sk, max(w.seqused_k[b], 0))
         last = sk - 1 if w.last_valid_kv_index < 0 else min(w.last_valid_kv_index, sk - 1)
         qs = np.arange(sq) if rows is None else np.asarray(
             [r - w.cu_seqlens_q[b] for r in rows if w.cu_seqlens_q[b] <= r < w.cu_seqlens_q[b + 1]])
@@ -58,7 +60,9 @@ def flops_of(w, rows=None) -> float:
             vis = np.full(len(qs), last + 1)
         else:
             off = w.prefix_offset if w.mask == wl.MASK_PREFIX_CAUSAL else 0
-            vis = np.clip(np.minimum(qs + off, last) + 1, 0, None)
+            hi = np.minimum(qs + off, last)
+            lo = np.maximum(qs + off - w.window_left, 0) if w.window_left >= 0 else 0
+            vis = np.clip(hi - lo + 1, 0, None)
         total += int(vis.sum())
     return 2.0 * total * w.H * (w.d_qk + w.d_v)
 

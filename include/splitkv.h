@@ -62,7 +62,9 @@ typedef enum { SK_BF16 = 0, SK_F16 = 1, SK_F32 = 2 } sk_dtype;
 
 /* [P1] Technical details: under causal and prefix-causal masking key j is visible to
  * query q when j <= q + prefix_offset (prefix_offset is 0 for plain causal);
- * under every mask j must also be <= lastValid. */
+ * under every mask j must also be <= lastValid. A sliding window (window_left >= 0)
+ * also hides keys before q + prefix_offset - window_left; it changes neither the
+ * per-row counts nor the partition (leading splits of a row then hold nothing). */
 typedef enum { SK_MASK_NONE = 0, SK_MASK_CAUSAL = 1, SK_MASK_PREFIX_CAUSAL = 2 } sk_mask;
 
 /* A [rows, heads, dim] (varlen) or [batch, rows, heads, dim] (dense) tensor with a
@@ -98,6 +100,14 @@ typedef struct {
                                     kernel merge the splits itself (the last CTA of each M
                                     block), instead of the separate combine; 0 (default)
                                     keeps the combine kernel, which measured faster */
+    int window_left;             /* -1: no sliding window; else (causal / prefix-causal masks
+                                    only) key j is visible to query q only if
+                                    j >= q + prefix_offset - window_left ([P2] Technical
+                                    details: the forced split honours the caller's window) */
+    const int32_t *seqused_k;    /* device int32 [B] or NULL: padded key slots -- sequence b
+                                    uses only its first seqused_k[b] keys; the rest of its
+                                    cu_seqlens / max_seqlen slot is padding ([P2] Technical
+                                    details: padded cu_seqlens) */
 } sk_params;
 
 /* Largest split_kv accepted. */

@@ -52,7 +52,8 @@ class _Params(ctypes.Structure):
                 ("mask", ctypes.c_int), ("prefix_offset", ctypes.c_int),
                 ("last_valid_kv_index", ctypes.c_int), ("n_per_block", ctypes.c_int),
                 ("split_kv", ctypes.c_int), ("block_m", ctypes.c_int),
-                ("softmax_scale", ctypes.c_float), ("fuse_combine", ctypes.c_int)]
+                ("softmax_scale", ctypes.c_float), ("fuse_combine", ctypes.c_int),
+                ("window_left", ctypes.c_int), ("seqused_k", ctypes.c_void_p)]
 
 
 class _Tensor(ctypes.Structure):
@@ -121,6 +122,8 @@ class Params:
     block_m: int = 0
     softmax_scale: float = 0.0
     fuse_combine: int = 0
+    window_left: int = -1
+    seqused_k: torch.Tensor | None = None
 
     def c(self) -> _Params:
         def ptr(t):
@@ -133,7 +136,8 @@ class Params:
                        self.total_k, self.d_qk, self.d_v, ptr(self.cu_seqlens_q),
                        ptr(self.cu_seqlens_k), self.mask, self.prefix_offset,
                        self.last_valid_kv_index, self.n_per_block, self.split_kv, self.block_m,
-                       self.softmax_scale, self.fuse_combine)
+                       self.softmax_scale, self.fuse_combine, self.window_left,
+                       ptr(self.seqused_k))
 
     @property
     def dense(self) -> bool:
@@ -148,7 +152,10 @@ def params_for(w, device="cuda", split_kv=None, **overrides) -> Params:
                total_q=w.total_q, total_k=w.total_k, d_qk=w.d_qk, d_v=w.d_v, cu_seqlens_q=cu_q,
                cu_seqlens_k=cu_k, mask=w.mask, prefix_offset=w.prefix_offset,
                last_valid_kv_index=w.last_valid_kv_index, n_per_block=w.n_per_block,
-               split_kv=w.split_kv if split_kv is None else split_kv)
+               split_kv=w.split_kv if split_kv is None else split_kv,
+               window_left=w.window_left,
+               seqused_k=None if w.seqused_k is None
+               else torch.tensor(w.seqused_k, dtype=torch.int32, device=device))
     for k_, v_ in overrides.items():
         setattr(p, k_, v_)
     return p

@@ -75,8 +75,18 @@ __global__ void __launch_bounds__(kThreads, NR <= 4 ? 2 : 1)
     if (R <= 0) return;
     int kb, ke;
     split_key_range(p, si.sq, si.last_valid, 0, s, kb, ke);
-    const int n_tiles = ke > kb ? (ke - kb + kKT - 1) / kKT : 0;
+    int n_tiles = ke > kb ? (ke - kb + kKT - 1) / kKT : 0;
     if (!DIRECT && n_tiles == 0 && p.skip_empty) return;  // real early exit: nothing is read
+    {
+        // sliding window: skip key tiles before row 0's window (the earliest of all rows)
+        const long long first = row_start(p, 0);
+        if (first > kb) {
+            int skip = (int)((first - kb) / kKT);
+            if (skip > n_tiles) skip = n_tiles;
+            kb += skip * kKT;
+            n_tiles -= skip;
+        }
+    }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
@@ -146,6 +156,9 @@ __global__ void __launch_bounds__(kThreads, NR <= 4 ? 2 : 1)
     const int kl = lane >> 2;          // key of the warp's 8 in this tile
     const int dq = lane & 3;           // quarter of the dot product
     int kend[NR];
+    long long kfirst[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) kfirst[r] = row_start(p, r);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
         int e = kb;  // rows past the sequence see nothing
@@ -218,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, NR <= 4 ? 2 : 1)
             float x = sc[r];
             x += __shfl_xor_sync(0xffffffffu, x, 1);
             x += __shfl_xor_sync(0xffffffffu, x, 2);
-            x = kidx < kend[r] ? x : -INFINITY;
+            x = (kidx < kend[r] && kidx >= kfirst[r]) ? x : -INFINITY;
             float tmax = x;
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
             tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));

@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kThreads)
         split_key_range(p, si.sq, si.last_valid, pos, s, kb, ke);
         long long lim = row_limit(p, si.last_valid, pos);
         if (lim + 1 < ke) ke = (int)(lim + 1 > kb ? lim + 1 : kb);
+        const long long first = row_start(p, pos);  // sliding window
+        if (first > kb) kb = (int)(first < ke ? first : ke);
     }
     if (tid == 0) { sRange[0] = INT_MAX; sRange[1] = 0; }
     // stage Q (widened) while the range is being reduced

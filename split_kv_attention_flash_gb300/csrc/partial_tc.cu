@@ -228,9 +228,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (pos0 >= si.sq) return;  // uniform: the M block lies past this sequence
     int kb, ke;
     split_key_range(p, si.sq, si.last_valid, pos0, s, kb, ke);
-    const int n_tiles = ke > kb ? (ke - kb + kBN - 1) / kBN : 0;
+    int n_tiles = ke > kb ? (ke - kb + kBN - 1) / kBN : 0;
     // real early exit: a split without keys writes nothing (the merge never reads it)
     if (!DIRECT && n_tiles == 0 && p.skip_empty && tickets == nullptr) return;
+    {
+        // sliding window: key tiles before the first key any row of the block may see
+        // (row pos0 has the earliest window) are skipped by every role
+        const long long first = row_start(p, pos0);
+        if (first > kb) {
+            int skip = (int)((first - kb) / kBN);
+            if (skip > n_tiles) skip = n_tiles;
+            kb += skip * kBN;
+            n_tiles -= skip;
+        }
+    }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
@@ -431,6 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + 256u + (uint32_t)t * 128u;
         const long long lim = row_limit(p, si.last_valid, pos);
         const int kend = lim + 1 < ke ? (int)(lim + 1 > kb ? lim + 1 : kb) : ke;
+        const long long kfirst = row_start(p, pos);  // sliding window (0 without one)
         const float sl2 = p.scale_log2;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
@@ -441,10 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[128];
             ptx::tmem_ld_x128(tS, r);
             const int nvalid = kend - (kb + j * kBN);
-            if (nvalid < kBN) {
+            const long long nlow = kfirst - (kb + (long long)j * kBN);
+            if (nvalid < kBN || nlow > 0) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (c >= nvalid) r[c] = __float_as_uint(-INFINITY);
+                    if (c >= nvalid || c < nlow) r[c] = __float_as_uint(-INFINITY);
             }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll

@@ -56,6 +56,8 @@ sk_status check_params(const sk_params *p) {
     if (!(p->softmax_scale == p->softmax_scale) || isinf(p->softmax_scale))
         return SK_ERR_INVALID_ARG;
     if (p->fuse_combine != 0 && p->fuse_combine != 1) return SK_ERR_INVALID_ARG;
+    if (p->window_left < -1 || (p->window_left >= 0 && p->mask == SK_MASK_NONE))
+        return SK_ERR_INVALID_ARG;
     if (!sk_supported_head_dims(p->d_qk, p->d_v)) return SK_ERR_UNSUPPORTED;
     return SK_OK;
 }
@@ -110,6 +112,8 @@ sk::Problem make_problem(const sk_params *p, int S) {
     pr.scale = p->softmax_scale != 0.f ? p->softmax_scale : (float)(1.0 / sqrt((double)p->d_qk));
     pr.scale_log2 = (float)((double)pr.scale * 1.4426950408889634074);
     pr.err = device_error_word();
+    pr.window_left = p->window_left;
+    pr.seqused_k = p->seqused_k;
     return pr;
 }
 

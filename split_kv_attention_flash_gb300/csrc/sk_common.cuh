@@ -29,6 +29,8 @@ struct Problem {
     float scale_log2;            // scale * log2(e): scores are kept in base 2
     int *err;                    // device error word (bounded waits), may be null
     int skip_empty;              // 1: split CTAs with no key exit without writing (sk_attn_fwd)
+    int window_left;             // -1: none; else keys before q + offset - window_left are hidden
+    const int32_t *seqused_k;    // device; null, or keys used per sequence (padded slots)
 };
 
 // A [rows, heads, dim] view with element strides (dense layout adds stride_b).
@@ -67,6 +69,10 @@ __device__ inline SeqInfo seq_info(const Problem &p, int b) {
     s.k0 = (int)k0;
     s.sq = clamp_len(q0, q1 - q0, p.max_sq, p.total_q);
     s.sk = clamp_len(k0, k1 - k0, p.max_sk, p.total_k);
+    if (p.seqused_k) {  // padded slot: only the first seqused_k[b] keys belong to the sequence
+        const int used = __ldg(p.seqused_k + b);
+        if (used < s.sk) s.sk = used < 0 ? 0 : used;
+    }
     int last = s.sk - 1;
     if (p.last_valid_kv_index >= 0 && p.last_valid_kv_index < last) last = p.last_valid_kv_index;
     s.last_valid = last;
@@ -153,6 +159,13 @@ __device__ inline long long row_limit(const Problem &p, int last_valid, int pos)
         if (c < lim) lim = c;
     }
     return lim;
+}
+
+// First key query `pos` may see under a sliding window (0 without one).
+__device__ inline long long row_start(const Problem &p, int pos) {
+    if (!p.causal || p.window_left < 0) return 0;
+    const long long x = (long long)pos + p.prefix_offset - p.window_left;
+    return x < 0 ? 0 : x;
 }
 
 // ---------------------------------------------------------------- conversions

@@ -41,6 +41,8 @@ class Workload:
     prefix_offset: int = 0
     last_valid_kv_index: int = -1
     value_scale: float = 1.0        # inputs are N(0, 1) * value_scale
+    window_left: int = -1           # sliding window (causal masks only), -1: none
+    seqused_k: tuple | None = None  # keys used per sequence when key slots are padded
     extra: dict = field(default_factory=dict, compare=False)
 
     @property
@@ -143,5 +145,10 @@ DECODE = Workload("decode bf16 (B32 H32 Sq1, Sk ~ U[4096, 131072], D128)", H=32,
 TARGET_D128 = TARGET_SHAPE.with_(name="varlen prefill bf16 Sq4096 Sk42700 H12 D128/128 non-causal",
                                  d_qk=128, d_v=128)
 
-ALL = {"tiny": TINY_CAUSAL, "noncausal": NONCAUSAL_BF16, "masked": MASKED_F16,
+# sliding-window prefill: the last 4096 queries of a 42700-key context, each seeing the
+# 8192 keys up to its own position
+WINDOW = TARGET_SHAPE.with_(name="sliding-window prefill bf16 Sq4096 Sk42700 H12 D192/128 window 8192",
+                            mask=MASK_PREFIX_CAUSAL, prefix_offset=42700 - 4096, window_left=8191)
+
+ALL = {"window": WINDOW, "tiny": TINY_CAUSAL, "noncausal": NONCAUSAL_BF16, "masked": MASKED_F16,
        "varlen": LONG_VARLEN, "target": TARGET_SHAPE, "decode": DECODE, "target_d128": TARGET_D128}

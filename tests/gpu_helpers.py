@@ -24,7 +24,9 @@ def oracle_problem(w, S: int, block_m: int | None = None) -> oracle.Problem:
     return oracle.Problem(cu_q=w.cu_seqlens_q, cu_k=w.cu_seqlens_k, H=w.H, d_qk=w.d_qk,
                           d_v=w.d_v, mask=w.mask, prefix_offset=w.prefix_offset,
                           last_valid_kv_index=w.last_valid_kv_index, n_per_block=w.n_per_block,
-                          split_kv=S, block_m=block_m or skv.sk_default_block_m(w.d_qk, w.d_v))
+                          split_kv=S, block_m=block_m or skv.sk_default_block_m(w.d_qk, w.d_v),
+                          window_left=w.window_left,
+                          seqused_k=None if w.seqused_k is None else list(w.seqused_k))
 
 
 def resolved_split(w, dev) -> int:

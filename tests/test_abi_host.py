@@ -76,6 +76,8 @@ def _fwd(L, p, q=None, k=None, v=None, out=None, ws=FAKE, ws_bytes=1 << 40):
     (dict(block_m=-4), SK_ERR_INVALID_ARG),
     (dict(softmax_scale=float("nan")), SK_ERR_INVALID_ARG),
     (dict(fuse_combine=2), SK_ERR_INVALID_ARG),
+    (dict(window_left=-2), SK_ERR_INVALID_ARG),
+    (dict(window_left=16), SK_ERR_INVALID_ARG),                 # a window needs a causal mask
     (dict(d_qk=96, d_v=96), SK_ERR_UNSUPPORTED),
     (dict(d_qk=128, d_v=64), SK_ERR_UNSUPPORTED),
 ])

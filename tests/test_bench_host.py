@@ -27,6 +27,14 @@ def test_flop_counts_of_the_workloads():
     assert bench.flops_of(fully_masked) == 2 * 16 * 256 * sum(max(0, q - 256 + 1) for q in range(2048))
 
 
+def test_flop_count_with_window_and_padding():
+    w = wl.Workload("w", H=1, seqlens_q=(10,), seqlens_k=(20,), d_qk=64, d_v=64, dtype="bf16",
+                    seed=0, mask=wl.MASK_PREFIX_CAUSAL, prefix_offset=5, window_left=3,
+                    seqused_k=(12,))
+    vis = sum(len([j for j in range(12) if q + 5 - 3 <= j <= q + 5]) for q in range(10))
+    assert bench.flops_of(w) == 2 * vis * 128
+
+
 def test_combine_bytes():
     w = wl.TARGET_SHAPE
     counts = np.full(w.total_q, 3, dtype=np.int32)

@@ -28,11 +28,15 @@ def _lib():
 
 
 def _small(dtype, dqk, dv, mask=wl.MASK_NONE, po=0, lvi=-1, bn=64, S=3, seed=0,
-           sq=(300, 1, 77, 256), sk=(1000, 5, 0, 513)):
-    return wl.Workload(f"small {dtype} {dqk}/{dv} mask{mask} po{po} lvi{lvi} S{S}", H=2,
-                       seqlens_q=sq, seqlens_k=sk, d_qk=dqk, d_v=dv, dtype=dtype, seed=seed,
-                       n_per_block=bn, split_kv=S, mask=mask, prefix_offset=po,
-                       last_valid_kv_index=lvi)
+           sq=(300, 1, 77, 256), sk=(1000, 5, 0, 513), window=-1, used=None):
+    name = f"small {dtype} {dqk}/{dv} mask{mask} po{po} lvi{lvi} S{S}"
+    if window >= 0:
+        name += f" window{window}"
+    if used is not None:
+        name += " padded"
+    return wl.Workload(name, H=2, seqlens_q=sq, seqlens_k=sk, d_qk=dqk, d_v=dv, dtype=dtype,
+                       seed=seed, n_per_block=bn, split_kv=S, mask=mask, prefix_offset=po,
+                       last_valid_kv_index=lvi, window_left=window, seqused_k=used)
 
 
 SMALL = [
@@ -44,6 +48,15 @@ SMALL = [
     _small("f32", 192, 128, mask=wl.MASK_CAUSAL, lvi=200, S=8, bn=48),
     _small("bf16", 64, 64, S=1),
     _small("bf16", 192, 128, S=7, bn=128, sq=(1, 1, 1), sk=(3000, 17, 0)),
+    # sliding windows and padded key slots (per-sequence used counts)
+    _small("bf16", 192, 128, mask=wl.MASK_CAUSAL, S=4, bn=128, window=300),
+    _small("f16", 128, 128, mask=wl.MASK_PREFIX_CAUSAL, po=500, S=3, bn=64, window=100,
+           used=(900, 5, 0, 400)),
+    _small("bf16", 128, 128, S=5, bn=128, sq=(1, 1, 1, 2), sk=(3000, 70, 500, 900),
+           used=(2500, 80, 3, 0)),
+    _small("bf16", 64, 64, mask=wl.MASK_PREFIX_CAUSAL, po=2000, S=6, bn=128, window=700,
+           sq=(1, 3, 16), sk=(3000, 2500, 2100)),
+    _small("f32", 128, 128, mask=wl.MASK_CAUSAL, S=3, bn=32, window=40, used=(800, 5, 0, 300)),
 ]
 
 
