@@ -1,7 +1,7 @@
 """Benchmark of the split-KV attention forward on GB300.
 
-One step = one sk_attn_fwd over the workload (split counts -> partial kernel ->
-combine), inputs resident in HBM. Default workload: the long-context varlen
+One step = one sk_attn_fwd over the workload (partial kernel -> combine, which
+evaluates the split-count formula itself), inputs resident in HBM. Default workload: the long-context varlen
 prefill target shape (bf16, Sq 4096, Sk 42700, H 12, D_QK 192, D_V 128,
 non-causal, split_kv automatic -> 3). Inputs (347 MB) are larger than L2.
 
@@ -224,7 +224,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         skv.sk_attn_fwd(p, q, k, v, out, lse, ws)
 
     fused = bool(p.fuse_combine) and kname == "partial_tc" and S <= 8
-    launches_per_step = 1 if S == 1 or fused else 3   # counts, partial, combine
+    launches_per_step = 1 if S == 1 or fused else 2   # partial, combine
     sampler = ClockSampler(dev.index)
     with sampler:
         for _ in range(args.warmup):

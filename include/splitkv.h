@@ -156,11 +156,12 @@ sk_status sk_combine(const sk_params *p, const float *o_part, const float *lse_p
                      const int32_t *counts, sk_tensor out, float *lse_out, sk_stream stream);
 
 /*
- * sk_attn_fwd -- the whole forward pass in one call: counts, partials, combine.
- * With S == 1 the partial kernel writes `out` and `lse_out` directly and no
- * workspace is used. With S > 1, splits that hold no key of their M block write
- * nothing (a real early exit) and the merge skips them. Otherwise `workspace` (device, 256-byte aligned, at least
- * sk_workspace_bytes()) holds the counts and the partials. max_seqlen_k == 0 writes
+ * sk_attn_fwd -- the whole forward pass in one call: partials, then the merge with
+ * the per-row counts. With S == 1 the partial kernel writes `out` and `lse_out`
+ * directly and no workspace is used. With S > 1, `workspace` (device, 256-byte
+ * aligned, at least sk_workspace_bytes()) holds the split partials; the combine
+ * evaluates the per-row count formula itself, and splits that hold no key of their
+ * M block write nothing (a real early exit) and are not read. max_seqlen_k == 0 writes
  * O = 0 and LSE = -inf ([P2] review: forced split with empty K must not raise;
  * [P1]: an empty split's LSE is -inf). lse_out may be NULL.
  */

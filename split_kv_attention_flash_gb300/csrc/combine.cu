@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
         const int r = warp * kRowsPerWarp + i;
-        cnt[i] = r < nrows ? merged_splits(p, si.sq, si.last_valid, pos0 + r, __ldg(counts + row0 + r)) : 0;
+        cnt[i] = r < nrows ? merged_splits(p, si.sq, si.last_valid, pos0 + r, row_count(p, si, counts, pos0 + r)) : 0;
     }
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     // ---- weights: warp 0, one lane per row
     if (warp == 0) {
         const int r = lane;
-        const int c = r < nrows ? merged_splits(p, si.sq, si.last_valid, pos0 + r, __ldg(counts + row0 + r)) : 0;
+        const int c = r < nrows ? merged_splits(p, si.sq, si.last_valid, pos0 + r, row_count(p, si, counts, pos0 + r)) : 0;
         const float *lrow = lse_part + (int64_t)h * S * plane + row0 + r;
         float m = -FLT_MAX;  // max(max_s L_s, lowest finite)
         for (int s = 0; s < c; ++s) {
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kBulkThreads)
 
     if (warp == 0) {
         const int c = lane < nrows
-                          ? merged_splits(p, si.sq, si.last_valid, pos0 + lane, __ldg(counts + row0 + lane))
+                          ? merged_splits(p, si.sq, si.last_valid, pos0 + lane, row_count(p, si, counts, pos0 + lane))
                           : 0;
         sCnt[lane] = c;
         int cmax = c;

@@ -132,17 +132,17 @@ sk_status cuda_status(cudaError_t e) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WorkspaceLayout {
-    size_t counts, o_part, lse_part, tickets, ticket_bytes, total;
+    size_t o_part, lse_part, tickets, ticket_bytes, total;
 };
 
-// counts | O_part | L_part | tickets (one int per (sequence, head, 256-row M block), for
-// the merge fused into the tensor-core kernel), each 256-byte aligned
+// O_part | L_part | tickets (one int per (sequence, head, 256-row M block), for the
+// merge fused into the tensor-core kernel), each 256-byte aligned. The counts need no
+// room: the combine evaluates their formula.
 WorkspaceLayout layout_for(const sk_params *p, int S) {
     WorkspaceLayout w{};
     if (S <= 1) return w;
     const size_t rows = (size_t)p->total_q;
-    w.counts = 0;
-    w.o_part = align256(rows * 4);
+    w.o_part = 0;
     w.lse_part = w.o_part + align256((size_t)p->H * S * rows * p->d_v * 4);
     w.tickets = w.lse_part + align256((size_t)p->H * S * rows * 4);
     w.ticket_bytes = (size_t)p->B * p->H * (((size_t)p->max_seqlen_q + 255) / 256) * 4;
@@ -290,7 +290,6 @@ sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
         return cuda_status(sk::run_partial(pr, q.dtype, view(q), view(k), view(v), nullptr,
                                            nullptr, &ov, lse_out, cs));
     char *ws = (char *)workspace;
-    int32_t *counts = (int32_t *)(ws + w.counts);
     float *o_part = (float *)(ws + w.o_part);
     float *lse_part = (float *)(ws + w.lse_part);
     if (p->fuse_combine && pr.bm == 256) {
@@ -303,13 +302,12 @@ sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
                                       lse_out, tickets, cs, &fused);
         if (e != cudaSuccess || fused) return cuda_status(e);
     }
-    cudaError_t e = sk::launch_counts(pr, counts, cs);
     sk::Problem pe = pr;
-    pe.skip_empty = 1;  // splits without keys write nothing; the combine never reads them
-    if (e == cudaSuccess)
-        e = sk::run_partial(pe, q.dtype, view(q), view(k), view(v), o_part, lse_part, nullptr,
-                            nullptr, cs);
-    if (e == cudaSuccess) e = sk::launch_combine(pr, out.dtype, o_part, lse_part, counts, ov, lse_out, cs);
+    pe.skip_empty = 1;     // splits without keys write nothing; the combine never reads them
+    pe.counts_inline = 1;  // the combine evaluates the per-row count formula itself
+    cudaError_t e = sk::run_partial(pe, q.dtype, view(q), view(k), view(v), o_part, lse_part,
+                                    nullptr, nullptr, cs);
+    if (e == cudaSuccess) e = sk::launch_combine(pe, out.dtype, o_part, lse_part, nullptr, ov, lse_out, cs);
     return cuda_status(e);
 }
 

@@ -29,6 +29,7 @@ struct Problem {
     float scale_log2;            // scale * log2(e): scores are kept in base 2
     int *err;                    // device error word (bounded waits), may be null
     int skip_empty;              // 1: split CTAs with no key exit without writing (sk_attn_fwd)
+    int counts_inline;           // 1: the combine evaluates the count formula itself (sk_attn_fwd)
     int window_left;             // -1: none; else keys before q + offset - window_left are hidden
     const int32_t *seqused_k;    // device; null, or keys used per sequence (padded slots)
 };
@@ -148,6 +149,11 @@ __device__ inline int merged_splits(const Problem &p, int sq, int last_valid, in
     int c = count < 1 ? 1 : (count > p.S ? p.S : count);
     const int ne = nonempty_splits(p, sq, last_valid, pos);
     return c < ne ? c : ne;
+}
+
+// The count of packed row q0 + pos: the caller's array, or the formula itself.
+__device__ inline int row_count(const Problem &p, const SeqInfo &si, const int32_t *counts, int pos) {
+    return p.counts_inline ? valid_split_count(p, si.last_valid, pos) : __ldg(counts + si.q0 + pos);
 }
 
 // Last key query `pos` may see, ignoring the split: lastValid, and q + offset

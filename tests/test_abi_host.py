@@ -110,8 +110,8 @@ def test_workspace_layout_sizes(L):
     for S, tq, H, dv in ((3, 100, 4, 128), (8, 16384, 12, 128), (2, 1, 1, 64)):
         p = _params(split_kv=S, total_q=tq, H=H, d_qk=dv, d_v=dv)
         tickets = p.B * H * ((p.max_seqlen_q + 255) // 256) * 4
-        assert skv.sk_workspace_bytes(p) == (a256(4 * tq) + a256(4 * H * S * tq * dv)
-                                            + a256(4 * H * S * tq) + a256(tickets))
+        assert skv.sk_workspace_bytes(p) == (a256(4 * H * S * tq * dv) + a256(4 * H * S * tq)
+                                            + a256(tickets))
     assert skv.sk_workspace_bytes(_params(split_kv=1)) == 0
 
 
