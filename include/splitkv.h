@@ -227,6 +227,13 @@ const char *sk_status_string(sk_status s);
  * on the calling thread, 0 if there was none; *name (optional) receives its name. */
 int sk_last_cuda_error(const char **name);
 
+/* Self-test of the give-up path of the kernels' bounded waits: launches one CTA that
+ * waits, through the same helper, on a barrier nothing arrives on, with a limit of
+ * timeout_ns (at most 2e9); the wait runs out, the CTA records code 0x401 in the device
+ * error word and returns. Read it with sk_read_device_error (SK_ERR_TIMEOUT). Larger
+ * limits return SK_ERR_INVALID_ARG without a launch. */
+sk_status sk_selftest_bounded_wait(unsigned long long timeout_ns, sk_stream stream);
+
 /* Debug: reads (and optionally clears) the device error word that bounded waits
  * set when they give up. SYNCHRONISES the current device. *code = 0: no error. */
 sk_status sk_read_device_error(int *code, int clear);

@@ -266,6 +266,13 @@ def sk_last_cuda_error() -> tuple[int, str]:
     return code, (name.value or b"").decode()
 
 
+def sk_selftest_bounded_wait(timeout_ns: int, stream=None):
+    fn = lib().sk_selftest_bounded_wait
+    fn.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+    _ok(fn(timeout_ns, _stream(stream) if torch.cuda.is_available() else None),
+        "sk_selftest_bounded_wait")
+
+
 def sk_read_device_error(clear: bool = True) -> int:
     code = ctypes.c_int()
     lib().sk_read_device_error(ctypes.byref(code), int(clear))

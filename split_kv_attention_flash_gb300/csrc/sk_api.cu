@@ -311,6 +311,13 @@ sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
     return cuda_status(e);
 }
 
+sk_status sk_selftest_bounded_wait(unsigned long long timeout_ns, sk_stream stream) {
+    if (timeout_ns > 2000000000ull) return SK_ERR_INVALID_ARG;
+    int *err = device_error_word();
+    if (!err) return SK_ERR_CUDA;
+    return cuda_status(sk::launch_selftest_wait(err, timeout_ns, (cudaStream_t)stream));
+}
+
 sk_status sk_read_device_error(int *code, int clear) {
     if (!code) return SK_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return SK_ERR_CUDA;

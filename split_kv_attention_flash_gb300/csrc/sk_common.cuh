@@ -223,6 +223,7 @@ cudaError_t launch_partial_decode(const Problem &p, int dtype, const TensorView 
                                   float *lse_part, const TensorView *out, float *lse_out,
                                   cudaStream_t st, bool *launched);
 }  // namespace dec
+cudaError_t launch_selftest_wait(int *err, unsigned long long timeout_ns, cudaStream_t st);
 cudaError_t launch_combine(const Problem &p, int dtype, const float *o_part,
                            const float *lse_part, const int32_t *counts, const TensorView &out,
                            float *lse_out, cudaStream_t st);

@@ -150,6 +150,12 @@ def test_auto_split_rules(L):
     assert skv.sk_choose_split_kv(p, 152) == 3
 
 
+def test_selftest_limit_is_checked_before_any_launch(L):
+    fn = L.sk_selftest_bounded_wait
+    fn.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+    assert fn(3_000_000_000, None) == SK_ERR_INVALID_ARG
+
+
 def test_status_strings(L):
     for code in range(6):
         assert skv.sk_status_string(code)
