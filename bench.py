@@ -99,9 +99,11 @@ def measured_peaks() -> dict:
     return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, valid only while the
-    kernel's source file is unchanged (its sha256 is recorded beside the number)."""
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary (profiles/traffic.txt), valid
+    only while the kernel's source file is unchanged (its sha256 prefix is recorded
+    beside the number). A line for another workload of the same kernel carries
+    `scale_<workload>=` factors when the traffic grows in proportion to the work."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -109,13 +111,28 @@ def recorded_traffic(kernel: str):
         f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
         if f.get("kernel") != kernel or "source" not in f:
             continue
+        if f.get("workload") == workload:
+            scale = 1.0
+        elif f"scale_{workload}" in f:
+            scale = float(f[f"scale_{workload}"])
+        else:
+            continue
         src = os.path.join(ROOT, f["source"])
         if not os.path.exists(src):
             continue
         if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != f.get("sha256"):
             return None
-        return float(f["dram_bytes_per_launch"]) * float(f.get("scale", 1.0))
+        return float(f["dram_bytes_per_launch"]) * scale
     return None
+
+
+def kv_bytes_of(w) -> float:
+    """Bytes of K and V a streaming kernel reads once: every used key of every head."""
+    keys = 0
+    for b in range(w.B):
+        sk = w.seqlens_k[b] if w.seqused_k is None else min(w.seqlens_k[b], max(w.seqused_k[b], 0))
+        keys += sk
+    return float(keys * w.H * (w.d_qk + w.d_v) * (4 if w.dtype == "f32" else 2))
 
 
 class ClockSampler:
@@ -306,7 +323,18 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     counts_np = counts.cpu().numpy()
     cbytes = combine_bytes(w, counts_np, with_lse=False)
     part_tflops = fl / (part_ms * 1e-3) / 1e12
-    traffic = recorded_traffic(kname)
+    traffic = recorded_traffic(kname, args.workload)
+    if kname == "partial_decode":   # a stream over K and V: bound by HBM
+        gbs = kv_bytes_of(w) / (part_ms * 1e-3) / 1e9
+        roofline = {"kernel": kname, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
+                    "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                    "peak_source": f"{peaks['source']} HBM copy", "ms_per_launch": part_ms,
+                    "bytes_per_launch": kv_bytes_of(w), "traffic": traffic}
+    else:
+        roofline = {"kernel": kname, "bound": "tensor", "achieved": part_tflops,
+                    "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": part_tflops / peaks["bf16"],
+                    "peak_source": f"{peaks['source']} dense bf16 burst",
+                    "ms_per_launch": part_ms, "flop_per_launch": fl, "traffic": traffic}
     line = {
         "metric": METRIC, "value": whole_job_tflops(fl, world, ms), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -320,12 +348,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
                    "flop_per_step": fl, "l2": "inputs larger than L2 "
                    f"({(q.numel() + k.numel() + v.numel()) * q.element_size() / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": kname, "bound": "tensor", "achieved": part_tflops,
-                     "peak": peaks["bf16"], "unit": "TFLOP/s",
-                     "frac": part_tflops / peaks["bf16"],
-                     "peak_source": f"{peaks['source']} dense bf16 burst",
-                     "ms_per_launch": part_ms,
-                     "traffic": traffic},
+        "roofline": roofline,
         "combine": {"achieved": cbytes / (comb_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "peak": peaks["hbm"], "frac": cbytes / (comb_ms * 1e-3) / 1e9 / peaks["hbm"],
                     "bytes": cbytes, "us_per_launch": comb_ms * 1e3, "l2": "flushed"},
