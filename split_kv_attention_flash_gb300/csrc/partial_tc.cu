@@ -37,13 +37,11 @@
 #include "sk_common.cuh"
 #include "sm100_ptx.cuh"
 #include "sk_dispatch.h"
+#include "tc_softmax.cuh"
 
 namespace sk {
 namespace tc {
 
-constexpr int kBM = 256;         // query rows per CTA
-constexpr int kTileM = 128;      // rows per MMA tile
-constexpr int kBN = 128;         // keys per MMA tile
 constexpr int kThreads = 384;    // softmax warpgroups 0, 1; warpgroup 2: producer, MMA, 2 idle
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -55,12 +53,7 @@ constexpr int kSoftmaxRegs = 208;
 constexpr int kControlRegs = 88;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch budget");
-constexpr int kChunkBytes = 128 * 128;  // one 64-column (128-byte) swizzled panel of 128 rows
-constexpr uint64_t kTimeoutNs = 1000000000ull;
-constexpr float kRescaleThreshold = 8.f;  // log2 units: rescale O only when m grows by > 2^8
 constexpr int kMinQueries = 17;           // fewer queries per sequence go to the CUDA-core kernel
-
-enum ErrCode : int { kErrProducer = 0x101, kErrMma = 0x102, kErrSoftmax = 0x103 };
 
 template <int DQK, int DV> struct Cfg {
     static constexpr int kQBytes = kTileM * DQK * 2;
@@ -89,30 +82,6 @@ template <int DQK, int DV> struct Cfg {
     static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "head dims");
     static_assert(kSplitV == (DQK == 192), "the V tensor map's box rows follow this rule");
 };
-
-// Wait of a whole warp: every lane polls, the warp leaves together.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int *err, int code) {
-    const int lane = threadIdx.x & 31;
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        bool ok = ptx::mbar_try_wait(bar, parity);
-        if (__all_sync(0xffffffffu, ok)) return true;
-        if ((i & 63u) == 63u) {
-            int give_up = 0;
-            if (lane == 0) {
-                if (t0 == 0) t0 = ptx::globaltimer();
-                if (*abort) give_up = 1;
-                else if (ptx::globaltimer() - t0 > kTimeoutNs) {
-                    *abort = 1;
-                    if (err) atomicCAS(err, 0, code);
-                    give_up = 1;
-                }
-            }
-            if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
-        }
-    }
-}
 
 constexpr int kMaxFusedSplits = 8;
 constexpr int kMergeBatch = 8;  // rows a warp loads at once
@@ -434,128 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------------------- softmax
         ptx::regs_inc<kSoftmaxRegs>();
-        const int t = warp >> 2, wq = warp & 3;
-        const int pos = pos0 + t * kTileM + wq * 32 + lane;
-        const bool row_ok = pos < si.sq;
-        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_off + (uint32_t)t * 128u;
-        const uint32_t tO = tmem + lane_off + 256u + (uint32_t)t * 128u;
-        const long long lim = row_limit(p, si.last_valid, pos);
-        const int kend = lim + 1 < ke ? (int)(lim + 1 > kb ? lim + 1 : kb) : ke;
-        const long long kfirst = row_start(p, pos);  // sliding window (0 without one)
-        const float sl2 = p.scale_log2;
-        float m = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            ok = warp_wait(bar(C::kBarS + t), j & 1, abort_flag, p.err, kErrSoftmax);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            uint32_t r[128];
-            ptx::tmem_ld_x128(tS, r);
-            const int nvalid = kend - (kb + j * kBN);
-            const long long nlow = kfirst - (kb + (long long)j * kBN);
-            if (nvalid < kBN || nlow > 0) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c >= nvalid || c < nlow) r[c] = __float_as_uint(-INFINITY);
-            }
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(r[c + u]));
-            }
-            const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            const float m_new = fmaxf(m, tmax * sl2);
-            const bool grow = m_new > m + kRescaleThreshold;  // also true for the first finite max
-            const bool any_grow = __any_sync(0xffffffffu, grow);
-            const float alpha = grow ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
-            if (grow) m = m_new;
-            l *= alpha;
-            const float mneg = m == -INFINITY ? 0.f : -m;
-            // p = 2^(s * scale * log2 e - m), two columns per packed FMA
-            const uint64_t sc2 = ptx::f2pack(sl2, sl2), mn2 = ptx::f2pack(mneg, mneg);
-            uint64_t sum2[2] = {0ull, 0ull};
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float a, bq;
-                ptx::f2unpack(ptx::ffma2(ptx::f2pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])),
-                                         sc2, mn2),
-                              a, bq);
-                a = ptx::ex2(a);
-                bq = ptx::ex2(bq);
-                sum2[c & 1] = ptx::fadd2(sum2[c & 1], ptx::f2pack(a, bq));
-                r[c] = ptx::pack2(a, bq, kBF16);
-            }
-            {
-                float s0, s1, s2, s3;
-                ptx::f2unpack(sum2[0], s0, s1);
-                ptx::f2unpack(sum2[1], s2, s3);
-                l += (s0 + s1) + (s2 + s3);
-            }
-            if (any_grow && j > 0) {
-                // warp-uniform (TMEM loads and stores are warp-collective). O_t holds the
-                // P V of tiles < j: S_t(j) completing implies PV_t(j-1) did.
-#pragma unroll
-                for (int c0 = 0; c0 < DV; c0 += 32) {
-                    uint32_t o[32];
-                    ptx::tmem_ld_x32(tO + c0, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    ptx::tmem_st_x32(tO + c0, o);
-                }
-            }
-            __syncwarp();
-            ptx::tmem_st_x64(tS, *reinterpret_cast<uint32_t(*)[64]>(r));
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(C::kBarP + t));
-        }
-        if (ok && n_tiles > 0) ok = warp_wait(bar(C::kBarO + t), 0, abort_flag, p.err, kErrSoftmax);
-        if (ok) {
-            ptx::tc_fence_after();
-            const bool empty = !(l > 0.f);
-            const float inv = empty ? 0.f : 1.f / l;
-            const float lse = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
-            const int row = si.q0 + pos;
-#pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 32) {
-                uint32_t o[32];
-                if (n_tiles > 0) ptx::tmem_ld_x32(tO + c0, o);
-                else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0u;
-                }
-                if (row_ok) {
-                if constexpr (DIRECT) {
-                    T *dst = (T *)out.ptr + row_offset(p, out, b, si.q0, pos) + (int64_t)h * out.sh + c0;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint4 v;
-                        v.x = ptx::pack2(__uint_as_float(o[i + 0]) * inv, __uint_as_float(o[i + 1]) * inv, kBF16);
-                        v.y = ptx::pack2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv, kBF16);
-                        v.z = ptx::pack2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv, kBF16);
-                        v.w = ptx::pack2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv, kBF16);
-                        *(uint4 *)(dst + i) = v;
-                    }
-                } else {
-                    float *dst = o_part + (((int64_t)h * p.S + s) * p.total_q + row) * DV + c0;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *(float4 *)(dst + i) = make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                                                           __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
-                }
-                }
-                __syncwarp();
-            }
-            if (row_ok) {
-                if constexpr (DIRECT) {
-                    if (lse_out) lse_out[(int64_t)h * p.total_q + row] = lse;
-                } else {
-                    lse_part[((int64_t)h * p.S + s) * p.total_q + row] = lse;
-                }
-            }
-        }
+        const int t = warp >> 2;
+        const SoftmaxBars sb{bar(C::kBarS + t), bar(C::kBarP + t), bar(C::kBarO + t)};
+        softmax_rows<T, DV, DIRECT>(p, si, b, h, s, pos0, t, tmem, kb, ke, n_tiles, sb,
+                                           abort_flag, o_part, lse_part, out, lse_out);
         if constexpr (!DIRECT) {
             // Fused merge: the CTA of this (sequence, head, M block) that writes its
             // partials last merges all splits. Every softmax thread takes part in both
@@ -613,7 +464,7 @@ static EncodeTiledFn encode_fn() {
 
 // [rows, H, D] (varlen: rows = total, one batch) or [B][rows][H][D] (dense), box of
 // 64 elements x box_rows rows, 128-byte swizzle; out-of-range rows read as zero.
-static bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long long rows, int H,
+bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long long rows, int H,
                      int B, bool dense, unsigned box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc || rows <= 0 || t.sr <= 0 || t.sh <= 0) return false;

@@ -7,6 +7,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -215,6 +216,10 @@ cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, 
                               const TensorView &v, float *o_part, float *lse_part,
                               const TensorView *out, float *lse_out, int *tickets, cudaStream_t st,
                               bool *launched);
+// TMA map of a [rows, H, D] (varlen) or [B][rows][H][D] (dense) 16-bit tensor: boxes of
+// 64 elements x box_rows rows, 128-byte swizzle. False when TMA cannot describe it.
+bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long long rows, int H, int B,
+              bool dense, unsigned box_rows);
 }  // namespace tc
 namespace dec {
 bool partial_decode_supported(const Problem &p, int dtype);

@@ -57,6 +57,12 @@ SMALL = [
     _small("bf16", 64, 64, mask=wl.MASK_PREFIX_CAUSAL, po=2000, S=6, bn=128, window=700,
            sq=(1, 3, 16), sk=(3000, 2500, 2100)),
     _small("f32", 128, 128, mask=wl.MASK_CAUSAL, S=3, bn=32, window=40, used=(800, 5, 0, 300)),
+    # unmasked, two or more M blocks: CTA pairs sharing each MMA, including pairs whose
+    # second block lies past its sequence, padded key slots, lastValid and S = 1
+    _small("f16", 192, 128, S=2, bn=128, sq=(600, 257, 3), sk=(900, 1300, 40)),
+    _small("bf16", 192, 128, S=3, bn=128, sq=(520, 300), sk=(2000, 700), used=(1800, 1)),
+    _small("f16", 128, 128, lvi=600, S=4, bn=64, sq=(700,), sk=(1500,)),
+    _small("bf16", 192, 128, S=1, bn=128, sq=(513, 40), sk=(1000, 3000)),
 ]
 
 
@@ -156,26 +162,28 @@ def test_combine_never_reads_invalid_splits(w):
     assert not torch.isnan(out2.float()).any()
 
 
-def test_dense_layout_equals_varlen():
-    w = wl.Workload("dense", H=3, seqlens_q=(130, 130), seqlens_k=(400, 400), d_qk=128, d_v=128,
-                    dtype="bf16", seed=9, n_per_block=64, split_kv=3, mask=wl.MASK_CAUSAL)
+@pytest.mark.parametrize("mask,sq", [(wl.MASK_CAUSAL, 130), (wl.MASK_NONE, 300)])
+def test_dense_layout_equals_varlen(mask, sq):
+    w = wl.Workload("dense", H=3, seqlens_q=(sq, sq), seqlens_k=(400, 400), d_qk=128, d_v=128,
+                    dtype="bf16", seed=9, n_per_block=64, split_kv=3, mask=mask)
     (_, _, _), (qd, kd, vd) = _inputs(w)
     out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
     p = skv.params_for(w, DEV)
     p.cu_seqlens_q = p.cu_seqlens_k = None
-    qb = qd.view(2, 130, 3, 128)
+    qb = qd.view(2, sq, 3, 128)
     kb, vb = kd.view(2, 400, 3, 128), vd.view(2, 400, 3, 128)
-    outb = torch.empty(2, 130, 3, 128, dtype=qd.dtype, device=DEV)
-    lseb = torch.empty(3, 260, dtype=torch.float32, device=DEV)
+    outb = torch.empty(2, sq, 3, 128, dtype=qd.dtype, device=DEV)
+    lseb = torch.empty(3, 2 * sq, dtype=torch.float32, device=DEV)
     ws = torch.empty(skv.sk_workspace_bytes(p), dtype=torch.uint8, device=DEV)
     skv.sk_attn_fwd(p, qb, kb, vb, outb, lseb, ws)
     torch.cuda.synchronize()
     assert torch.equal(outb.view_as(out), out) and torch.equal(lseb, lse)
 
 
-def test_strided_heads_and_rows():
+@pytest.mark.parametrize("mask", [wl.MASK_CAUSAL, wl.MASK_NONE])
+def test_strided_heads_and_rows(mask):
     """Q/K/V as views into wider buffers (row stride > H * d)."""
-    w = _small("bf16", 128, 128, mask=wl.MASK_CAUSAL, S=3)
+    w = _small("bf16", 128, 128, mask=mask, S=3)
     (q, k, v), (qd, kd, vd) = _inputs(w)
     pad = 8
     def widen(t):
