@@ -66,8 +66,16 @@ __global__ void __launch_bounds__(kThreads, NR <= 4 ? 2 : 1)
                           float *lse_out) {
     using C = Cfg<DQK, DV>;
     extern __shared__ uint8_t smem_raw[];
-    const int h = blockIdx.y;
-    const int s = blockIdx.x % p.S, b = blockIdx.x / p.S;
+    // CTA i of the launch order (x fastest) takes head i % H of the unit of rank i / H
+    // in longest-first order (the ring's memory serves as scratch before any load)
+    int h = blockIdx.y, unit = blockIdx.x;
+    if (gridDim.x > 1 && gridDim.x <= kLptMaxUnits) {
+        const int i = blockIdx.x + blockIdx.y * gridDim.x;
+        h = i % p.H;
+        int *scratch = (int *)smem_raw;
+        unit = lpt_unit(p, i / p.H, gridDim.x, scratch, scratch + kLptMaxUnits);
+    }
+    const int s = unit % p.S, b = unit / p.S;
     const SeqInfo si = seq_info(p, b);
     // NR (a power of two >= every sequence's query count) rows are computed; rows at or
     // past this sequence's count are masked out and never stored

@@ -134,6 +134,39 @@ __host__ __device__ inline void split_key_range(const Problem &p, int sq, int la
 // first ceil(tiles / itersPerBlock) of them. The merge never reads the others ([P1]
 // review notes on a real early exit: a split with nothing to do may write nothing,
 // so the merge must not assume its memory was written).
+// Longest-first launch order. The CTAs of a (sequence, split) unit all stream that
+// split's keys; with sequences of very different lengths, launching the units in
+// index order can leave the longest ones for the last wave. lpt_unit returns the unit
+// of rank r when the n units are sorted by their key count, largest first (ties by
+// index), so that a CTA's rank in the hardware's launch order picks its unit. Every
+// thread of the CTA calls it; `keys` is shared memory for n ints, `found` one int.
+constexpr int kLptMaxUnits = 256;
+__device__ inline int unit_keys(const Problem &p, int u) {
+    const int b = u / p.S, s = u % p.S;
+    const SeqInfo si = seq_info(p, b);
+    if (si.sq <= 0) return -1;
+    int kb, ke;
+    split_key_range(p, si.sq, si.last_valid, ((si.sq - 1) / p.bm) * p.bm, s, kb, ke);
+    return ke > kb ? ke - kb : 0;
+}
+__device__ inline int lpt_unit(const Problem &p, int r, int n, int *keys, int *found) {
+    for (int u = threadIdx.x; u < n; u += blockDim.x) keys[u] = unit_keys(p, u);
+    __syncthreads();
+    for (int u = threadIdx.x; u < n; u += blockDim.x) {
+        const int ku = keys[u];
+        int rank = 0;
+        for (int v = 0; v < n; ++v) {
+            const int kv = keys[v];
+            rank += (kv > ku) | ((kv == ku) & (v < u));
+        }
+        if (rank == r) *found = u;
+    }
+    __syncthreads();
+    const int u = *found;
+    __syncthreads();  // the scratch may be reused from here on
+    return u;
+}
+
 __host__ __device__ inline int nonempty_splits(const Problem &p, int sq, int last_valid, int pos) {
     long long first = (long long)(pos / p.bm) * p.bm;
     long long last_row = first + p.bm - 1;
