@@ -11,9 +11,10 @@
 //
 // combine_bulk_kernel (S <= 8): a CTA merges 32 consecutive rows of one head. For a
 // (head, split) plane those rows are one contiguous chunk of 32 * d_v floats, so one
-// thread issues one bulk asynchronous copy per split into shared memory (splits up
-// to the largest count of the 32 rows) while warp 0 forms the weights; then every
-// warp merges 8 rows out of shared memory.
+// thread first issues one bulk asynchronous copy per split into shared memory (the
+// splits the partition leaves non-empty for the M block), then warp 0 forms the
+// counts and weights while they land; then every warp merges 8 rows out of shared
+// memory.
 //
 // combine_kernel (any S <= 32): a CTA merges 32 consecutive rows of one head:
 //   * every warp reads the counts of its 4 rows and at once issues the 16-byte
@@ -162,7 +163,6 @@ __global__ void __launch_bounds__(kBulkThreads)
     __shared__ float sW[kBulkMaxSplits][kBulkRows];
     __shared__ float sInv[kBulkRows];
     __shared__ int sCnt[kBulkRows];
-    __shared__ int sMax;
     __shared__ volatile int sAbort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -178,33 +178,27 @@ __global__ void __launch_bounds__(kBulkThreads)
     const uint32_t bar = ptx::smem_u32(&sBar);
     const float *sO = (const float *)sO_raw;
 
-    if (warp == 0) {
-        const int c = lane < nrows
-                          ? merged_splits(p, si.sq, si.last_valid, pos0 + lane, row_count(p, si, counts, pos0 + lane))
-                          : 0;
-        sCnt[lane] = c;
-        int cmax = c;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-        if (lane == 0) {
-            sMax = cmax;
-            sAbort = 0;
-            ptx::mbar_init(bar, 1);
-            ptx::fence_mbar_init();
-        }
-    }
-    __syncthreads();
-    const int nsplit = sMax;
     if (tid == 0) {
+        // the copies start first: the splits the block partition leaves non-empty for this
+        // M block bound every row's merged count (and are the ones the partial kernel wrote)
+        sAbort = 0;
+        ptx::mbar_init(bar, 1);
+        ptx::fence_mbar_init();
+        const int ne = nonempty_splits(p, si.sq, si.last_valid, pos0);
         const uint32_t chunk = (uint32_t)nrows * DV * 4;
-        ptx::mbar_arrive_expect_tx(bar, chunk * (uint32_t)nsplit);
-        for (int sp = 0; sp < nsplit; ++sp)
+        ptx::mbar_arrive_expect_tx(bar, chunk * (uint32_t)ne);
+        for (int sp = 0; sp < ne; ++sp)
             ptx::bulk_load(ptx::smem_u32(sO_raw) + (uint32_t)sp * kBulkRows * DV * 4,
                            o_part + (((int64_t)h * S + sp) * plane + row0) * DV, chunk, bar);
     }
     if (warp == 0) {
-        // weights, one lane per row: m = max(max_s L_s, lowest finite), w_s = exp(L_s - m)
-        const int r = lane, c = sCnt[r];
+        // one lane per row: its merged count, then m = max(max_s L_s, lowest finite),
+        // w_s = exp(L_s - m)
+        const int r = lane;
+        const int c = r < nrows
+                          ? merged_splits(p, si.sq, si.last_valid, pos0 + r, row_count(p, si, counts, pos0 + r))
+                          : 0;
+        sCnt[r] = c;
         const float *lrow = lse_part + (int64_t)h * S * plane + row0 + r;
         float l[kBulkMaxSplits];
         float m = -FLT_MAX;

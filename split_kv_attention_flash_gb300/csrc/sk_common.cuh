@@ -100,13 +100,18 @@ __host__ __device__ inline long long covered_last(const Problem &p, int last_val
 }
 
 // [P1] per-row valid-split count (computeValidSplitKV).
+// ceil(a / b) for b >= 1 in 32-bit unsigned arithmetic (a - 1 avoids the overflow of
+// a + b - 1); the quantities below stay under 2^32: n <= 2^31 and bn * tiles < n + bn.
+__host__ __device__ inline uint32_t ceil_div_u32(uint32_t a, uint32_t b) {
+    return a == 0 ? 0u : (a - 1u) / b + 1u;
+}
 __host__ __device__ inline int valid_split_count(const Problem &p, int last_valid, int pos) {
     long long rl = covered_last(p, last_valid, pos);
     if (rl < 0) return 1;
-    long long n = rl + 1;
-    long long tiles = (n + p.bn - 1) / p.bn;
-    long long kps = (long long)p.bn * ((tiles + p.S - 1) / p.S);
-    return (int)((n + kps - 1) / kps);
+    const uint32_t n = (uint32_t)rl + 1u;
+    const uint32_t tiles = ceil_div_u32(n, (uint32_t)p.bn);
+    const uint32_t kps = (uint32_t)p.bn * ceil_div_u32(tiles, (uint32_t)p.S);
+    return (int)ceil_div_u32(n, kps);
 }
 
 // Keys [kb, ke) of split s for the M block that holds query `pos` ([P1]: the kernel
@@ -120,8 +125,8 @@ __host__ __device__ inline void split_key_range(const Problem &p, int sq, int la
     long long bl = covered_last(p, last_valid, last_row);
     kb = ke = 0;
     if (bl < 0) return;
-    long long nt = (bl + p.bn) / p.bn;
-    long long it = (nt + p.S - 1) / p.S;
+    const long long nt = (uint32_t)bl / (uint32_t)p.bn + 1u;
+    const long long it = ceil_div_u32((uint32_t)nt, (uint32_t)p.S);
     long long t0 = (long long)s * it, t1 = t0 + it;
     if (t1 > nt) t1 = nt;
     if (t0 >= t1) return;
@@ -173,9 +178,9 @@ __host__ __device__ inline int nonempty_splits(const Problem &p, int sq, int las
     if (last_row > sq - 1) last_row = sq - 1;
     long long bl = covered_last(p, last_valid, last_row);
     if (bl < 0) return 0;
-    long long nt = (bl + p.bn) / p.bn;
-    long long it = (nt + p.S - 1) / p.S;
-    return (int)((nt + it - 1) / it);
+    const uint32_t nt = (uint32_t)bl / (uint32_t)p.bn + 1u;
+    const uint32_t it = ceil_div_u32(nt, (uint32_t)p.S);
+    return (int)ceil_div_u32(nt, it);
 }
 
 // Splits the merge reads for query `pos`: min(count, non-empty splits of its block).
