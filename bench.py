@@ -100,11 +100,24 @@ def measured_peaks() -> dict:
     return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
+def sources_sha(paths: list[str]) -> str | None:
+    """sha256 prefix of the concatenated files (a kernel's source and the headers it
+    includes), or None when one is missing."""
+    h = hashlib.sha256()
+    for rel in paths:
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary (profiles/traffic.txt), valid
-    only while the kernel's source file is unchanged (its sha256 prefix is recorded
-    beside the number). A line for another workload of the same kernel carries
-    `scale_<workload>=` factors when the traffic grows in proportion to the work."""
+    only while the kernel's sources are unchanged (the sha256 prefix of its source and
+    headers, `source=` a comma-separated list, is recorded beside the number). A line
+    for another workload of the same kernel carries `scale_<workload>=` factors when
+    the traffic grows in proportion to the work."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -118,10 +131,7 @@ def recorded_traffic(kernel: str, workload: str):
             scale = float(f[f"scale_{workload}"])
         else:
             continue
-        src = os.path.join(ROOT, f["source"])
-        if not os.path.exists(src):
-            continue
-        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != f.get("sha256"):
+        if sources_sha(f["source"].split(",")) != f.get("sha256"):
             return None
         return float(f["dram_bytes_per_launch"]) * scale
     return None

@@ -85,7 +85,9 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)t * 128u;
     const long long lim = row_limit(p, si.last_valid, pos);
     const int kend = lim + 1 < ke ? (int)(lim + 1 > kb ? lim + 1 : kb) : ke;
-    const long long kfirst = row_start(p, pos);  // sliding window (0 without one)
+    // sliding window: the row's first visible key (0 without one), at most ke
+    const long long kfirst_ll = row_start(p, pos);
+    const int kfirst = kfirst_ll < ke ? (int)kfirst_ll : ke;
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -96,7 +98,7 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
         uint32_t r[128];
         ptx::tmem_ld_x128(tS, r);
         const int nvalid = kend - (kb + j * kBN);
-        const long long nlow = kfirst - (kb + (long long)j * kBN);
+        const int nlow = kfirst - (kb + j * kBN);
         if (nvalid < kBN || nlow > 0) {
 #pragma unroll
             for (int c = 0; c < 128; ++c)

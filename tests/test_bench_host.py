@@ -90,3 +90,20 @@ def test_reference_arm_runs_on_rank_zero_only():
     class Args:
         workload, steps, warmup, cpu_seconds, gpus = "tiny", 1, 3, 1.0, 2
     assert bench.run_reference(Args, rank=1) is None
+
+
+def test_recorded_traffic_lines_name_existing_sources():
+    """Every profiles/traffic.txt line names sources that exist; a line whose sources still
+    hash to its recorded prefix yields its bytes (scaled for another workload), any other
+    line yields None rather than a stale number."""
+    path = os.path.join(bench.ROOT, "profiles", "traffic.txt")
+    for line in open(path):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        srcs = f["source"].split(",")
+        assert all(os.path.exists(os.path.join(bench.ROOT, s)) for s in srcs)
+        got = bench.recorded_traffic(f["kernel"], f["workload"])
+        if bench.sources_sha(srcs) == f["sha256"]:
+            assert got == float(f["dram_bytes_per_launch"])
+        else:
+            assert got is None
+    assert bench.recorded_traffic("partial_tc", "no such workload") is None
