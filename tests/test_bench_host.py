@@ -107,3 +107,10 @@ def test_recorded_traffic_lines_name_existing_sources():
         else:
             assert got is None
     assert bench.recorded_traffic("partial_tc", "no such workload") is None
+
+
+def test_vs_baseline_only_for_the_pages_workload():
+    assert abs(bench.vs_pages("target", bench.PAGES_SPLIT3_TFLOPS) - 1.0) < 1e-12
+    for name in wl.ALL:
+        if name != "target":
+            assert bench.vs_pages(name, 123.0) is None
