@@ -10,8 +10,9 @@
 // Design (GB300, one CTA per SM):
 //   * The M block is two 128-row MMA tiles Q0, Q1, kept in shared memory for the
 //     whole CTA (TMA, 128-byte swizzle). Keys stream through in tiles of 128.
-//   * Warp 8 (one lane) is the TMA producer: Q once, then K(j) and V(j) into
-//     rings of shared-memory stages guarded by full / empty mbarriers. With a single
+//   * Warps 8 and 10 (one lane each) are the TMA producers -- Q once and K(j);
+//     V(j) -- into rings of shared-memory stages guarded by full / empty mbarriers,
+//     so that a K stage is refilled as soon as it is free. With a single
 //     V stage (D_QK = 192, where Q takes 96 KB) the stage is two 64-key halves with
 //     their own barriers: PV1(j) frees the first half after its first four MMAs, so
 //     V(j+1) starts arriving before PV1(j) has finished.
@@ -42,9 +43,10 @@
 namespace sk {
 namespace tc {
 
-constexpr int kThreads = 384;    // softmax warpgroups 0, 1; warpgroup 2: producer, MMA, 2 idle
-constexpr int kProducerWarp = 8;
+constexpr int kThreads = 384;    // softmax warpgroups 0, 1; warpgroup 2: producers, MMA, 1 idle
+constexpr int kProducerWarp = 8;   // Q and K
 constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10; // V
 // Registers are allocated per SM sub-partition: with 12 warps a thread may start with
 // at most 168. Warpgroup 2 gives registers back and the softmax warpgroups take them:
 // 2 * 128 * 208 + 128 * 88 = 384 * 168, exactly the launch's budget.
@@ -257,62 +259,72 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= 8) {
     ptx::regs_dec<kControlRegs>();
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == kProducerWarp || warp == kVProducerWarp) {
+        // ---------------------------------------------------------- TMA producers
+        // Two threads: K (with Q) and V, so that K(j + 1) is requested as soon as its
+        // stage is free rather than after V(j), whose single stage frees late.
         if (lane == 0 && n_tiles > 0) {
-            ptx::prefetch_tensormap(&tmQ);
-            ptx::prefetch_tensormap(&tmK);
-            ptx::prefetch_tensormap(&tmV);
-            const int qrow = dense ? pos0 : si.q0 + pos0;
             const int krow = (dense ? 0 : si.k0) + kb;
-            ptx::mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kQBytes);
-            for (int t = 0; t < 2; ++t)
-                for (int c = 0; c < DQK / 64; ++c)
-                    ptx::tma_load_4d(sQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar(C::kBarQ),
-                                     c * 64, qrow + t * kTileM, h, cb);
-            int issued_k = 0, issued_v = 0;
+            int quiet = 0;
+            volatile int *no_abort = (volatile int *)&quiet;
             bool ok = true;
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int ks = j % C::kKStages, vs = j % C::kVStages;
-                ok = ptx::mbar_wait_bounded(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1,
-                                            abort_flag, p.err, kErrProducer, kTimeoutNs);
-                if (!ok) break;
-                ptx::mbar_arrive_expect_tx(bar(C::kBarKF + ks), C::kKBytes);
-                for (int c = 0; c < DQK / 64; ++c)
-                    ptx::tma_load_4d(sK + ks * C::kKBytes + c * kChunkBytes, &tmK,
-                                     bar(C::kBarKF + ks), c * 64, krow + j * kBN, h, cb);
-                issued_k = j + 1;
-                for (int hf = 0; hf < C::kVParts && ok; ++hf) {
-                    const int vb = C::kVParts * vs + hf;
-                    ok = ptx::mbar_wait_bounded(bar(C::kBarVE + vb), ((j / C::kVStages) & 1) ^ 1,
+            if (warp == kProducerWarp) {
+                ptx::prefetch_tensormap(&tmQ);
+                ptx::prefetch_tensormap(&tmK);
+                const int qrow = dense ? pos0 : si.q0 + pos0;
+                ptx::mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kQBytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int c = 0; c < DQK / 64; ++c)
+                        ptx::tma_load_4d(sQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar(C::kBarQ),
+                                         c * 64, qrow + t * kTileM, h, cb);
+                int issued_k = 0;
+                for (int j = 0; j < n_tiles; ++j) {
+                    const int ks = j % C::kKStages;
+                    ok = ptx::mbar_wait_bounded(bar(C::kBarKE + ks), ((j / C::kKStages) & 1) ^ 1,
                                                 abort_flag, p.err, kErrProducer, kTimeoutNs);
                     if (!ok) break;
-                    ptx::mbar_arrive_expect_tx(bar(C::kBarVF + vb), C::kVPartBytes);
-                    for (int c = 0; c < DV / 64; ++c)
-                        ptx::tma_load_4d(sV + vs * C::kVBytes + hf * C::kVPartBytes + c * C::kVPanelBytes,
-                                         &tmV, bar(C::kBarVF + vb), c * 64,
-                                         krow + j * kBN + hf * (kBN / C::kVParts), h, cb);
-                    issued_v = C::kVParts * j + hf + 1;
+                    ptx::mbar_arrive_expect_tx(bar(C::kBarKF + ks), C::kKBytes);
+                    for (int c = 0; c < DQK / 64; ++c)
+                        ptx::tma_load_4d(sK + ks * C::kKBytes + c * kChunkBytes, &tmK,
+                                         bar(C::kBarKF + ks), c * 64, krow + j * kBN, h, cb);
+                    issued_k = j + 1;
                 }
-                if (!ok) break;
-            }
-            if (!ok) {
-                // drain: every load already issued must land before the CTA exits
-                int quiet = 0;
-                volatile int *no_abort = (volatile int *)&quiet;
-                ptx::mbar_wait_bounded(bar(C::kBarQ), 0, no_abort, nullptr, 0, kTimeoutNs);
-                for (int i = 0; i < C::kKStages && i < issued_k; ++i) {
-                    const int last = i + ((issued_k - 1 - i) / C::kKStages) * C::kKStages;
-                    ptx::mbar_wait_bounded(bar(C::kBarKF + i), (last / C::kKStages) & 1, no_abort,
-                                           nullptr, 0, kTimeoutNs);
+                if (!ok) {
+                    // drain: every load already issued must land before the CTA exits
+                    ptx::mbar_wait_bounded(bar(C::kBarQ), 0, no_abort, nullptr, 0, kTimeoutNs);
+                    for (int i = 0; i < C::kKStages && i < issued_k; ++i) {
+                        const int last = i + ((issued_k - 1 - i) / C::kKStages) * C::kKStages;
+                        ptx::mbar_wait_bounded(bar(C::kBarKF + i), (last / C::kKStages) & 1, no_abort,
+                                               nullptr, 0, kTimeoutNs);
+                    }
                 }
-                // V parts are issued in the order P j, P j + 1, ... (P = kVParts) into
-                // barrier (j % kVStages) * P + part
-                constexpr int kVB = C::kVParts * C::kVStages;
-                for (int i = 0; i < kVB && i < issued_v; ++i) {
-                    const int last = i + ((issued_v - 1 - i) / kVB) * kVB;
-                    ptx::mbar_wait_bounded(bar(C::kBarVF + i), ((last / C::kVParts) / C::kVStages) & 1,
-                                           no_abort, nullptr, 0, kTimeoutNs);
+            } else {
+                ptx::prefetch_tensormap(&tmV);
+                int issued_v = 0;
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    const int vs = j % C::kVStages;
+                    for (int hf = 0; hf < C::kVParts; ++hf) {
+                        const int vb = C::kVParts * vs + hf;
+                        ok = ptx::mbar_wait_bounded(bar(C::kBarVE + vb), ((j / C::kVStages) & 1) ^ 1,
+                                                    abort_flag, p.err, kErrProducer, kTimeoutNs);
+                        if (!ok) break;
+                        ptx::mbar_arrive_expect_tx(bar(C::kBarVF + vb), C::kVPartBytes);
+                        for (int c = 0; c < DV / 64; ++c)
+                            ptx::tma_load_4d(sV + vs * C::kVBytes + hf * C::kVPartBytes + c * C::kVPanelBytes,
+                                             &tmV, bar(C::kBarVF + vb), c * 64,
+                                             krow + j * kBN + hf * (kBN / C::kVParts), h, cb);
+                        issued_v = C::kVParts * j + hf + 1;
+                    }
+                }
+                if (!ok) {
+                    // V parts are issued in the order P j, P j + 1, ... (P = kVParts) into
+                    // barrier (j % kVStages) * P + part
+                    constexpr int kVB = C::kVParts * C::kVStages;
+                    for (int i = 0; i < kVB && i < issued_v; ++i) {
+                        const int last = i + ((issued_v - 1 - i) / kVB) * kVB;
+                        ptx::mbar_wait_bounded(bar(C::kBarVF + i), ((last / C::kVParts) / C::kVStages) & 1,
+                                               no_abort, nullptr, 0, kTimeoutNs);
+                    }
                 }
             }
         }
@@ -399,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_wait_bounded(bar(C::kBarDrain), 0, (volatile int *)&dummy, nullptr, 0,
                                    kTimeoutNs);
         }
-    }  // warps 10 and 11 have no role
+    }  // warp 11 has no role
     } else {
         // ---------------------------------------------------------------- softmax
         ptx::regs_inc<kSoftmaxRegs>();
