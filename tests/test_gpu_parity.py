@@ -66,6 +66,27 @@ SMALL = [
 ]
 
 
+# limits and degenerate shapes: the largest split count, single-key and 256-key partition
+# tiles, many short sequences (some without queries or keys), many heads, lastValid = 0,
+# a one-key sliding window
+LIMITS = [
+    _small("bf16", 128, 128, mask=wl.MASK_CAUSAL, S=32, bn=16, sq=(300,), sk=(4000,)),
+    _small("bf16", 64, 64, mask=wl.MASK_CAUSAL, S=5, bn=1, sq=(100, 40), sk=(300, 57)),
+    _small("f16", 192, 128, S=3, bn=256, sq=(520,), sk=(3000,)),
+    wl.Workload("many short sequences", H=4,
+                seqlens_q=tuple(int(x) for x in np.random.default_rng(5).integers(0, 41, 64)),
+                seqlens_k=tuple(int(x) for x in np.random.default_rng(6).integers(0, 501, 64)),
+                d_qk=128, d_v=128, dtype="bf16", seed=5, n_per_block=16, split_kv=4,
+                mask=wl.MASK_PREFIX_CAUSAL, prefix_offset=20),
+    wl.Workload("many heads", H=64, seqlens_q=(260,), seqlens_k=(700,), d_qk=64, d_v=64,
+                dtype="bf16", seed=7, n_per_block=128, split_kv=2),
+    _small("bf16", 128, 128, S=3, bn=64, sq=(0, 70, 0, 300), sk=(50, 0, 900, 400)),
+    _small("bf16", 192, 128, S=4, bn=128, lvi=0, sq=(50, 300), sk=(1000, 10)),
+    _small("f16", 128, 128, mask=wl.MASK_PREFIX_CAUSAL, po=100, S=3, bn=64, window=0,
+           sq=(300, 17), sk=(800, 200)),
+]
+
+
 def _inputs(w):
     q, k, v = w.make_inputs("cpu")
     return (q, k, v), (q.to(DEV), k.to(DEV), v.to(DEV))
@@ -123,6 +144,30 @@ def test_forward_matches_oracle_small(w):
     # without an LSE output the output is identical
     out2, _, _ = H.run_fwd(w, qd, kd, vd, DEV, with_lse=False)
     assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("w", LIMITS, ids=lambda w: w.name)
+def test_limits_match_oracle(w):
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    S = H.resolved_split(w, DEV)
+    p = skv.params_for(w, DEV, split_kv=S)
+    counts = torch.full((w.total_q,), -7, dtype=torch.int32, device=DEV)
+    skv.sk_valid_split_counts(p, counts)
+    assert np.array_equal(counts.cpu().numpy(), oracle.split_counts(H.oracle_problem(w, S)))
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
+
+
+def test_long_single_sequence_sampled():
+    """One sequence of 262144 keys (well past the workloads' longest), sampled rows."""
+    w = wl.Workload("long single sequence", H=2, seqlens_q=(512,), seqlens_k=(262144,), d_qk=128,
+                    d_v=128, dtype="bf16", seed=8, n_per_block=128, split_kv=0, value_scale=0.5)
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    out, lse, p = H.run_fwd(w, qd, kd, vd, DEV)
+    rows = H.sample_rows(w, head=32, tail=32, rand=32)
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v, rows=rows)
+    H.assert_close(H.to_np(out, rows), H.lse_np(lse, rows), ref_o, ref_l, w.dtype, "forward")
 
 
 @pytest.mark.parametrize("w", SMALL[:4], ids=lambda w: w.name)
