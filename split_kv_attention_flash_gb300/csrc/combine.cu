@@ -9,11 +9,11 @@
 // The pass is HBM-bound: it reads count * (4 d_v + 4) bytes and writes d_v
 // storage-type elements (+ 4 bytes of LSE) per (head, row).
 //
-// combine_bulk_kernel (S <= 8): a CTA merges 32 consecutive rows of one head. For a
-// (head, split) plane those rows are one contiguous chunk of 32 * d_v floats, so one
+// combine_bulk_kernel (S <= 8): a CTA merges 16 consecutive rows of one head. For a
+// (head, split) plane those rows are one contiguous chunk of 16 * d_v floats, so one
 // thread first issues one bulk asynchronous copy per split into shared memory (the
 // splits the partition leaves non-empty for the M block), then warp 0 forms the
-// counts and weights while they land; then every warp merges 8 rows out of shared
+// counts and weights while they land; then every warp merges 4 rows out of shared
 // memory.
 //
 // combine_kernel (any S <= 32): a CTA merges 32 consecutive rows of one head:
@@ -145,13 +145,13 @@ __global__ void __launch_bounds__(kWarps * 32)
 }
 
 namespace {
-constexpr int kBulkRows = 32;
 constexpr int kBulkThreads = 128;
+constexpr int kBulkRowsDefault = 16;  // rows per CTA (measured: 32 and 8 were slower)
 constexpr int kBulkMaxSplits = 8;
 constexpr uint64_t kBulkTimeoutNs = 1000000000ull;
 }  // namespace
 
-template <typename TO, int DV>
+template <typename TO, int DV, int kBulkRows>
 __global__ void __launch_bounds__(kBulkThreads)
     combine_bulk_kernel(Problem p, const float *__restrict__ o_part,
                         const float *__restrict__ lse_part, const int32_t *__restrict__ counts,
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kBulkThreads)
             ptx::bulk_load(ptx::smem_u32(sO_raw) + (uint32_t)sp * kBulkRows * DV * 4,
                            o_part + (((int64_t)h * S + sp) * plane + row0) * DV, chunk, bar);
     }
-    if (warp == 0) {
+    if (warp == 0 && lane < kBulkRows) {
         // one lane per row: its merged count, then m = max(max_s L_s, lowest finite),
         // w_s = exp(L_s - m)
         const int r = lane;
@@ -249,11 +249,11 @@ __global__ void __launch_bounds__(kBulkThreads)
     }
 }
 
-template <typename TO, int DV>
+template <typename TO, int DV, int kBulkRows>
 static cudaError_t launch_bulk(const Problem &p, const float *o_part, const float *lse_part,
                                const int32_t *counts, const TensorView &out, float *lse_out,
                                cudaStream_t st) {
-    auto kern = combine_bulk_kernel<TO, DV>;
+    auto kern = combine_bulk_kernel<TO, DV, kBulkRows>;
     constexpr int kMaxSmem = kBulkMaxSplits * kBulkRows * DV * 4;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -278,8 +278,8 @@ static cudaError_t launch_dv(const Problem &p, const float *o_part, const float 
                              cudaStream_t st) {
     if (p.S > kMaxSplits) return cudaErrorInvalidValue;
     if (p.S <= kBulkMaxSplits) {
-        if (p.d_v == 128) return launch_bulk<TO, 128>(p, o_part, lse_part, counts, out, lse_out, st);
-        if (p.d_v == 64) return launch_bulk<TO, 64>(p, o_part, lse_part, counts, out, lse_out, st);
+        if (p.d_v == 128) return launch_bulk<TO, 128, kBulkRowsDefault>(p, o_part, lse_part, counts, out, lse_out, st);
+        if (p.d_v == 64) return launch_bulk<TO, 64, kBulkRowsDefault>(p, o_part, lse_part, counts, out, lse_out, st);
     }
     const int row_blocks = (p.max_sq + kRowsPerCta - 1) / kRowsPerCta;
     const long long nx = (long long)row_blocks * p.B;
