@@ -11,7 +11,7 @@
  * tests/test_oracle_pins.py: the worked split counts printed on [P1], the review
  * notes' conservativeness bound checked by brute force, closed forms of
  * attention, a library attention routine in double precision, and the identity
- * "merge of the partials == unsplit attention".
+ * that merging the partials gives unsplit attention.
  */
 #include "oracle.h"
 
@@ -169,8 +169,8 @@ int orc_split_counts(const orc_problem *p, int32_t *counts)
     return 0;
 }
 
-/* [P1] "The kernel partitions each M block's keys using the block's last row":
- * the block's key tiles 0 .. nT-1 (nT = ceil((blockLast + 1) / nPerBlock)) are
+/* [P1] Technical details, kernel partition: an M block's keys are split by the
+ * block's last row: the block's key tiles 0 .. nT-1 (nT = ceil((blockLast + 1) / nPerBlock)) are
  * dealt out in runs of itersPerBlock = ceil(nT / split_kv) tiles, split s taking
  * tiles [s * itersPerBlock, (s + 1) * itersPerBlock). Keys after blockLast are
  * masked for every row of the block, so the range stops at blockLast + 1. */
