@@ -335,6 +335,13 @@ def test_config_long_varlen_full():
     _sampled_check(w, [0, 2, 3, 4, 5, 6, 7, 8], rows_kw=dict(head=16, tail=16, rand=16))
 
 
+def test_target_shape_full():
+    """The benchmark's default workload in the launch it times: automatic split (3)."""
+    w = wl.TARGET_SHAPE
+    assert H.resolved_split(w, DEV) == 3
+    _sampled_check(w, [0, 3], rows_kw=dict(head=32, tail=32, rand=64))
+
+
 def test_config_decode_full():
     w = wl.DECODE
     _sampled_check(w, [0, 1, 2, 4, 8, 16, 32], seq_subset=[0, 7, 19, 31])
