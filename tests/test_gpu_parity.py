@@ -159,6 +159,22 @@ def test_limits_match_oracle(w):
     H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
 
 
+@pytest.mark.parametrize("w", [
+    _small("bf16", 192, 128, S=3, bn=128, sq=(520,), sk=(3000,)),
+    _small("f16", 128, 128, mask=wl.MASK_CAUSAL, S=4, bn=64, sq=(300,), sk=(900,)),
+], ids=lambda w: w.name)
+def test_large_logits_match_oracle(w):
+    """Q and K scaled by 6 (scores of a few hundred): the running max jumps within and across
+    key tiles, the lazy rescale of O fires, and a few keys dominate each row."""
+    (q, k, v), _ = _inputs(w)
+    q, k = (t.float().mul(6.0).to(t.dtype) for t in (q, k))
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    assert ref_l.max() > 100.0
+    out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
+
+
 def test_long_single_sequence_sampled():
     """One sequence of 262144 keys (well past the workloads' longest), sampled rows."""
     w = wl.Workload("long single sequence", H=2, seqlens_q=(512,), seqlens_k=(262144,), d_qk=128,
