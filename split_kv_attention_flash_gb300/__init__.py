@@ -5,8 +5,9 @@ computation runs in the library's CUDA kernels. PyTorch is used only for device
 memory and streams. The functions keep the C names:
 
   sk_valid_split_counts, sk_attn_partial_fwd, sk_combine, sk_attn_fwd,
-  sk_workspace_bytes, sk_auto_split_kv, sk_choose_split_kv, sk_default_block_m,
-  sk_partial_kernel_name, sk_status_string, sk_read_device_error
+  sk_attn_fwd_static, sk_workspace_bytes, sk_auto_split_kv, sk_choose_split_kv,
+  sk_default_block_m, sk_partial_kernel_name, sk_status_string, sk_last_cuda_error,
+  sk_selftest_bounded_wait, sk_read_device_error
 
 plus `attention(...)`, which allocates the output / workspace with torch and calls
 sk_attn_fwd (the one-call entry, with split_kv = 0 meaning automatic).
