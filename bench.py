@@ -144,6 +144,13 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
+def hbm_bound(flop: float, kv_bytes: float, peaks: dict) -> bool:
+    """Whether the partial kernel's roofline is HBM: fewer FLOPs per byte of K and V than
+    the ratio of the measured bf16 peak to the measured HBM copy bandwidth (decode shapes,
+    a few queries per sequence), rather than the tensor cores (prefill shapes)."""
+    return flop / max(kv_bytes, 1.0) < peaks["bf16"] * 1e12 / (peaks["hbm"] * 1e9)
+
+
 def kv_bytes_of(w) -> float:
     """Bytes of K and V a streaming kernel reads once: every used key of every head."""
     keys = 0
@@ -377,7 +384,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         part_ms = ms
     part_tflops = fl / (part_ms * 1e-3) / 1e12
     traffic = recorded_traffic(kname, args.workload)
-    if kname == "partial_decode":   # a stream over K and V: bound by HBM
+    if hbm_bound(fl, kv_bytes_of(w), peaks):   # a stream over K and V: bound by HBM
         gbs = kv_bytes_of(w) / (part_ms * 1e-3) / 1e9
         roofline = {"kernel": kname, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
                     "unit": "GB/s", "frac": gbs / peaks["hbm"],

@@ -3,9 +3,10 @@
 
 namespace sk {
 
-// Tensor cores (tcgen05) for 16-bit storage with the library's M block and more
-// than 16 queries in the longest sequence; the streaming decode kernel for 16-bit
-// storage with at most 16 queries per sequence; the CUDA-core kernel for the rest
+// Tensor cores (tcgen05) for 16-bit storage with the library's M block and at least
+// two queries in the longest sequence; the streaming decode kernel for 16-bit storage
+// with one query per sequence (and up to 16 when the tensor-core kernel does not
+// apply); the CUDA-core kernel for the rest
 // (f32 storage, other M blocks, no keys, tensors TMA cannot describe).
 const char *partial_kernel_name(const Problem &p, int dtype, const TensorView &q,
                                 const TensorView &k, const TensorView &v) {

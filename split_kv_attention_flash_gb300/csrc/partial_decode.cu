@@ -1,4 +1,5 @@
-// partial_decode.cu -- split partials for sequences of at most 16 queries (decode),
+// partial_decode.cu -- split partials for sequences of one query (decode; up to 16
+// when the tensor-core kernel does not apply),
 // bf16 / f16 storage.
 //
 // [P1] Summary / Technical details: O_s and L_s of one (sequence, head, split) over

@@ -150,8 +150,12 @@ TARGET_D128 = TARGET_SHAPE.with_(name="varlen prefill bf16 Sq4096 Sk42700 H12 D1
 WINDOW = TARGET_SHAPE.with_(name="sliding-window prefill bf16 Sq4096 Sk42700 H12 D192/128 window 8192",
                             mask=MASK_PREFIX_CAUSAL, prefix_offset=42700 - 4096, window_left=8191)
 
+# multi-token decode: eight queries per sequence (speculative or batched decoding)
+DECODE_MQ = DECODE.with_(name="multi-query decode bf16 (B32 H32 Sq8, Sk ~ U[4096, 131072], D128)",
+                         seqlens_q=(8,) * 32)
+
 # a 2 GB decode case with the decode workload's layout (for profiler captures)
 DECODE_SMALL = DECODE.with_(name="decode bf16 (B32 H32 Sq1, Sk 8192, D128)", seqlens_k=(8192,) * 32)
 
-ALL = {"decode_small": DECODE_SMALL, "window": WINDOW, "tiny": TINY_CAUSAL, "noncausal": NONCAUSAL_BF16, "masked": MASKED_F16,
+ALL = {"decode_small": DECODE_SMALL, "decode_mq": DECODE_MQ, "window": WINDOW, "tiny": TINY_CAUSAL, "noncausal": NONCAUSAL_BF16, "masked": MASKED_F16,
        "varlen": LONG_VARLEN, "target": TARGET_SHAPE, "decode": DECODE, "target_d128": TARGET_D128}

@@ -114,3 +114,11 @@ def test_vs_baseline_only_for_the_pages_workload():
     for name in wl.ALL:
         if name != "target":
             assert bench.vs_pages(name, 123.0) is None
+
+
+def test_roofline_bound_follows_the_arithmetic_intensity():
+    peaks = {"bf16": 1890.1, "hbm": 6770.5}
+    for name, hbm in (("target", False), ("varlen", False), ("decode", True), ("decode_mq", True),
+                      ("decode_small", True)):
+        w = wl.ALL[name]
+        assert bench.hbm_bound(bench.flops_of(w), bench.kv_bytes_of(w), peaks) == hbm, name

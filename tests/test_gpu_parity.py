@@ -175,6 +175,32 @@ def test_large_logits_match_oracle(w):
     H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
 
 
+@pytest.mark.parametrize("dtype,mask,po", [("bf16", wl.MASK_NONE, 0), ("f16", wl.MASK_PREFIX_CAUSAL, 700)])
+def test_decode_kernel_with_several_queries(dtype, mask, po):
+    """Up to 16 queries per sequence with an M block of 64 rows: the tensor-core kernel
+    (256-row M blocks) does not apply, so the CUDA-core decode kernel takes every query
+    count it is templated on (1, 2, 4, 8, 16)."""
+    w = _small(dtype, 128, 128, mask=mask, po=po, S=3, bn=64, sq=(1, 2, 3, 16, 8, 5),
+               sk=(900, 40, 0, 1000, 777, 300))
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    bm = 64
+    p = skv.params_for(w, DEV, split_kv=3, block_m=bm)
+    assert skv.sk_partial_kernel_name(p, qd, kd, vd) == "partial_decode"
+    o_part = torch.empty(w.H, 3, w.total_q, w.d_v, dtype=torch.float32, device=DEV)
+    l_part = torch.empty(w.H, 3, w.total_q, dtype=torch.float32, device=DEV)
+    skv.sk_attn_partial_fwd(p, qd, kd, vd, o_part, l_part)
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=qd.dtype, device=DEV)
+    lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(skv.sk_workspace_bytes(p), 1), dtype=torch.uint8, device=DEV)
+    skv.sk_attn_fwd(p, qd, kd, vd, out, lse, ws)
+    torch.cuda.synchronize()
+    ref_po, ref_pl = oracle.partials(H.oracle_problem(w, 3, block_m=bm), q, k, v)
+    H.assert_close(o_part.permute(2, 0, 1, 3).cpu().numpy(), l_part.permute(2, 0, 1).cpu().numpy(),
+                   ref_po, ref_pl, w.dtype, "partials")
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
+
+
 def test_long_single_sequence_sampled():
     """One sequence of 262144 keys (well past the workloads' longest), sampled rows."""
     w = wl.Workload("long single sequence", H=2, seqlens_q=(512,), seqlens_k=(262144,), d_qk=128,
