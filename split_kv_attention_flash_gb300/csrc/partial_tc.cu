@@ -186,7 +186,11 @@ __device__ __forceinline__ void merge_block(const Problem &p, const SeqInfo &si,
     }
 }
 
-template <typename T, int DQK, int DV, bool DIRECT>
+// LPT: the (sequence, split) units -- the slowest launch dimension -- are taken longest
+// first (lpt_unit). Only instantiated for single-M-block launches (decode-like shapes with
+// a few queries per sequence), where ragged sequence lengths would otherwise leave the
+// longest sequences for the last wave; prefill launches keep the unit from blockIdx.
+template <typename T, int DQK, int DV, bool DIRECT, bool LPT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, Problem p, float *o_part,
@@ -196,7 +200,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
 
     const int mb = blockIdx.x, h = blockIdx.y;
-    const int s = blockIdx.z % p.S, b = blockIdx.z / p.S;
+    int s, b;
+    if constexpr (LPT) {
+        __shared__ int lpt_found;
+        const int unit = lpt_unit(p, blockIdx.z, gridDim.z, (int *)smem_raw, &lpt_found);
+        s = unit % p.S;
+        b = unit / p.S;
+    } else {
+        // straight from the block index, which the compiler may re-read instead of keeping
+        s = blockIdx.z % p.S;
+        b = blockIdx.z / p.S;
+    }
     const SeqInfo si = seq_info(p, b);
     const int pos0 = mb * kBM;
     if (pos0 >= si.sq) return;  // uniform: the M block lies past this sequence
@@ -496,12 +510,12 @@ bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long long r
     return r == CUDA_SUCCESS;
 }
 
-template <typename T, int DQK, int DV, bool DIRECT>
+template <typename T, int DQK, int DV, bool DIRECT, bool LPT = false>
 static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                               const CUtensorMap &mv, float *o_part, float *lse_part,
                               const TensorView &out, float *lse_out, int *tickets, cudaStream_t st) {
     using C = Cfg<DQK, DV>;
-    auto kern = partial_tc_kernel<T, DQK, DV, DIRECT>;
+    auto kern = partial_tc_kernel<T, DQK, DV, DIRECT, LPT>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -524,6 +538,10 @@ static cudaError_t launch_dims(const Problem &p, const CUtensorMap &mq, const CU
                                const TensorView *out, float *lse_out, int *tickets, cudaStream_t st) {
     if (out && !tickets)
         return launch_cfg<T, DQK, DV, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out, nullptr, st);
+    const long long units = (long long)p.B * p.S;
+    if (!(out && tickets) && p.max_sq <= kBM && units > 1 && units <= kLptMaxUnits)
+        return launch_cfg<T, DQK, DV, false, true>(p, mq, mk, mv, o_part, lse_part, TensorView{}, nullptr,
+                                                   nullptr, st);
     return launch_cfg<T, DQK, DV, false>(p, mq, mk, mv, o_part, lse_part, out ? *out : TensorView{},
                                          out ? lse_out : nullptr, out ? tickets : nullptr, st);
 }
