@@ -203,7 +203,10 @@ sk_status sk_workspace_bytes(const sk_params *p, size_t *bytes);
  * max_seqlen_k >= 8192 (an explicit boundary, as the review asks) and
  * ceil(max_seqlen_q / block_m) * H <= 2 * SM count; otherwise 1. For single-query
  * problems (max_seqlen_q == 1) it takes the smallest S <= 32 with B * H * S >= 2 * SM
- * count. A non-zero split_kv is returned unchanged. Reads the current device.
+ * count. Under a sliding window (causal / prefix-causal masks) the result is 1 when the
+ * deepest query, max_seqlen_q - 1 + prefix_offset, sees no key of split 0 of that S: the
+ * partition has no window term, so the leading splits would only write empty partials.
+ * A non-zero split_kv is returned unchanged. Reads the current device.
  */
 sk_status sk_auto_split_kv(const sk_params *p, int *split_kv_out);
 

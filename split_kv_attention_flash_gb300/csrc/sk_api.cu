@@ -198,6 +198,23 @@ sk_status sk_choose_split_kv(const sk_params *p, int sm_count, int *split_kv_out
             long long q_tiles = ((long long)p->max_seqlen_q + bm - 1) / bm;
             if (p->max_seqlen_k >= 8192 && q_tiles * p->H <= 2LL * sm_count) S = 3;
         }
+        // The auto rule applies where the split kernel's contract matches ([P2] Technical
+        // details). The partition starts its splits at key 0 and has no window term, so a
+        // sliding window that hides the whole first split from the deepest query leaves
+        // that split (and often more) with nothing to do: keep such problems unsplit.
+        if (S > 1 && p->window_left >= 0 && p->mask != SK_MASK_NONE && p->n_per_block >= 1) {
+            const long long off = p->mask == SK_MASK_PREFIX_CAUSAL ? p->prefix_offset : 0;
+            const long long deepest = (long long)p->max_seqlen_q - 1 + off;
+            long long last = deepest < p->max_seqlen_k - 1 ? deepest : p->max_seqlen_k - 1;
+            if (p->last_valid_kv_index >= 0 && last > p->last_valid_kv_index)
+                last = p->last_valid_kv_index;
+            if (last >= 0) {
+                const long long nb = p->n_per_block;
+                const long long tiles = (last + nb) / nb;
+                const long long first_split_keys = nb * ((tiles + S - 1) / S);
+                if (deepest - p->window_left >= first_split_keys) S = 1;
+            }
+        }
     }
     *split_kv_out = S;
     return SK_OK;

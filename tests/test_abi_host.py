@@ -150,6 +150,34 @@ def test_auto_split_rules(L):
     assert skv.sk_choose_split_kv(p, 152) == 3
 
 
+def test_auto_split_keeps_windowed_problems_unsplit_when_the_first_split_is_hidden(L):
+    # the window workload: the last 4096 queries of 42700 keys, window 8192. Split 0 of 3
+    # holds keys [0, 14336); the deepest row's window starts at 42699 - 8191 = 34508.
+    base = dict(B=1, H=12, max_seqlen_q=4096, max_seqlen_k=42700, total_q=4096, total_k=42700,
+                split_kv=0, mask=2, prefix_offset=42700 - 4096, d_qk=192, d_v=128, n_per_block=128)
+    assert skv.sk_choose_split_kv(_params(**base), 152) == 3
+    assert skv.sk_choose_split_kv(_params(**base, window_left=8191), 152) == 1
+    # the boundary: the deepest window start equal to the first split's end hides it
+    assert skv.sk_choose_split_kv(_params(**base, window_left=42699 - 14336), 152) == 1
+    assert skv.sk_choose_split_kv(_params(**base, window_left=42699 - 14335), 152) == 3
+    # a window wider than the context hides nothing
+    assert skv.sk_choose_split_kv(_params(**base, window_left=50000), 152) == 3
+    # lastValid shortens the partition: 20000 keys in tiles of 128 give a first split of
+    # 128 * ceil(157 / 3) = 6784 keys; the window start 34508 is past it
+    assert skv.sk_choose_split_kv(_params(**base, window_left=8191, last_valid_kv_index=19999),
+                                  152) == 1
+    # plain causal ignores prefix_offset; Sq = Sk = 16384, first split 5504 keys
+    c = dict(B=1, H=4, max_seqlen_q=16384, max_seqlen_k=16384, total_q=16384, total_k=16384,
+             split_kv=0, mask=1, n_per_block=128)
+    assert skv.sk_choose_split_kv(_params(**c, window_left=16383 - 5504), 152) == 1
+    assert skv.sk_choose_split_kv(_params(**c, window_left=16383 - 5503), 152) == 3
+    # no mask: the window is not applied, nor is the rule
+    assert skv.sk_choose_split_kv(_params(**dict(base, mask=0, prefix_offset=0), window_left=10),
+                                  152) == 3
+    # a forced split is returned unchanged
+    assert skv.sk_choose_split_kv(_params(**dict(base, split_kv=4), window_left=8191), 152) == 4
+
+
 def test_selftest_limit_is_checked_before_any_launch(L):
     fn = L.sk_selftest_bounded_wait
     fn.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
