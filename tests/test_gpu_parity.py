@@ -389,6 +389,33 @@ def test_config_decode_full():
     _sampled_check(w, [0, 1, 2, 4, 8, 16, 32], seq_subset=[0, 7, 19, 31])
 
 
+def test_config_target_d128_full():
+    w = wl.TARGET_D128
+    assert H.resolved_split(w, DEV) == 3
+    _sampled_check(w, [0], rows_kw=dict(head=32, tail=32, rand=64))
+
+
+def test_config_window_full():
+    """The sliding-window workload: the window hides split 0 of 3 from the deepest rows, so
+    auto keeps it unsplit; forced splits leave the leading splits of those rows empty."""
+    w = wl.WINDOW
+    assert H.resolved_split(w, DEV) == 1
+    _sampled_check(w, [0, 2, 3], rows_kw=dict(head=32, tail=32, rand=64))
+
+
+def test_config_decode_mq_full():
+    """Eight queries per sequence go to the tensor-core kernel (auto: 3 splits)."""
+    w = wl.DECODE_MQ
+    assert H.resolved_split(w, DEV) == 3
+    _sampled_check(w, [0, 1, 4], seq_subset=[0, 7, 19, 31])
+
+
+def test_config_decode_small_full():
+    w = wl.DECODE_SMALL
+    assert H.resolved_split(w, DEV) == 1
+    _sampled_check(w, [0, 2], seq_subset=[0, 13, 31])
+
+
 @pytest.mark.parametrize("w", [SMALL[1], SMALL[2], SMALL[4], SMALL[-1]], ids=lambda w: w.name)
 def test_fused_merge_matches_separate_combine(w):
     """sk_attn_fwd with fuse_combine = 1 (the tensor-core kernel merges in the last CTA of
