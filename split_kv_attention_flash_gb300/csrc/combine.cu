@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kBulkThreads)
                         TensorView out, float *__restrict__ lse_out, int row_blocks) {
     static_assert(DV % 4 == 0 && DV / 4 <= 32, "one float4 per lane");
     constexpr int kLanes = DV / 4;
-    extern __shared__ __align__(128) uint8_t sO_raw[];   // [split][32 rows][DV] f32
+    extern __shared__ __align__(128) uint8_t sO_raw[];   // [split][kBulkRows rows][DV] f32
     __shared__ __align__(8) uint64_t sBar;
     __shared__ float sW[kBulkMaxSplits][kBulkRows];
     __shared__ float sInv[kBulkRows];
