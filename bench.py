@@ -401,11 +401,10 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": vs_pages(args.workload, whole_job_tflops(fl, world, ms)),
         "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "sequences": w.B, "seq_len_q": list(w.seqlens_q),
-                   "seq_len_k": list(w.seqlens_k), "heads": w.H, "d_qk": w.d_qk, "d_v": w.d_v,
-                   "split_kv": S, "n_per_block": w.n_per_block, "fuse_combine": p.fuse_combine,
+        "config": {**shape_config(w),
+                   "split_kv": S, "fuse_combine": p.fuse_combine,
                    "block_m": skv.sk_default_block_m(w.d_qk, w.d_v),
-                   "flop_per_step": fl, "l2": "inputs larger than L2 "
+                   "l2": "inputs larger than L2 "
                    f"({(q.numel() + k.numel() + v.numel()) * q.element_size() / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
@@ -425,6 +424,13 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(w, args.cpu_seconds)
     return line
+
+
+def shape_config(w) -> dict:
+    """The workload's shape keys of the JSON line's config, shared by both arms."""
+    return {"workload": w.name, "sequences": w.B, "seq_len_q": list(w.seqlens_q),
+            "seq_len_k": list(w.seqlens_k), "heads": w.H, "d_qk": w.d_qk, "d_v": w.d_v,
+            "n_per_block": w.n_per_block, "flop_per_step": flops_of(w)}
 
 
 def run_reference(args, rank: int):
@@ -448,7 +454,7 @@ def run_reference(args, rank: int):
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": vs_pages(args.workload, value), "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": w.name, "heads": w.H, "d_qk": w.d_qk, "d_v": w.d_v},
+            "config": {**shape_config(w), "parallelism": "host cores (the f64 oracle, unsplit)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": base["cores"],
                              "kind": "oracle", "sample": base["sample"] + " per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
