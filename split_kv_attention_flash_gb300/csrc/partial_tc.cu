@@ -434,8 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::regs_inc<kSoftmaxRegs>();
         const int t = warp >> 2;
         const SoftmaxBars sb{bar(C::kBarS + t), bar(C::kBarP + t), bar(C::kBarO + t)};
+        // epilogue staging: 4 KB per softmax warp in the K stages, which no load or MMA
+        // touches once the O-done barrier has completed (or when the split has no tile)
+        float4 *stage = (float4 *)(gen_base + (sK - sQ)) + warp * 256;
         softmax_rows<T, DV, DIRECT>(p, si, b, h, s, pos0, t, tmem, kb, ke, n_tiles, sb,
-                                           abort_flag, o_part, lse_part, out, lse_out);
+                                           abort_flag, o_part, lse_part, out, lse_out, stage);
         if constexpr (!DIRECT) {
             // Fused merge: the CTA of this (sequence, head, M block) that writes its
             // partials last merges all splits. Every softmax thread takes part in both

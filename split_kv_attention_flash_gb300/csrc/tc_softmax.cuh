@@ -74,7 +74,8 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
                                              int pos0, int t, uint32_t tmem, int kb, int ke,
                                              int n_tiles, const SoftmaxBars &bars,
                                              volatile int *abort_flag, float *o_part,
-                                             float *lse_part, const TensorView &out, float *lse_out) {
+                                             float *lse_part, const TensorView &out, float *lse_out,
+                                             float4 *stage) {
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3;
@@ -181,12 +182,29 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
                     v.w = ptx::pack2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv, kBF16);
                     *(uint4 *)(dst + i) = v;
                 }
-            } else {
-                float *dst = o_part + (((int64_t)h * p.S + s) * p.total_q + row) * DV + c0;
+            }
+        }
+        if constexpr (!DIRECT) {
+            // The warp's 32 rows x 32 columns go through its shared-memory slice, so that
+            // each store covers four whole 128-byte row segments instead of 16 bytes of 32
+            // rows. Slot k of row r sits at r * 8 + (k ^ (r & 7)): conflict-free both when
+            // a thread writes its row and when eight lanes read one row.
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *(float4 *)(dst + i) = make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                                                       __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+            for (int k = 0; k < 8; ++k)
+                stage[lane * 8 + (k ^ (lane & 7))] =
+                    make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+            __syncwarp();
+            const int k = lane & 7;
+            const int row_w = pos0 + t * kTileM + wq * 32;  // the warp's first row
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = it * 4 + (lane >> 3);
+                if (row_w + r < si.sq) {
+                    float *dst = o_part + (((int64_t)h * p.S + s) * p.total_q + si.q0 + row_w + r) * DV +
+                                 c0 + 4 * k;
+                    *(float4 *)dst = stage[r * 8 + (k ^ (r & 7))];
+                }
             }
         }
         __syncwarp();
