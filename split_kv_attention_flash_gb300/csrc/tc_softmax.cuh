@@ -162,52 +162,73 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
     const float inv = empty ? 0.f : 1.f / l;
     const float lse = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
     const int row = si.q0 + pos;
+    // The warp's rows leave through its shared-memory slice (32 rows x 128 bytes), so that
+    // each store covers four whole 128-byte row segments instead of 16 bytes of 32 rows.
+    // Slot k (16 bytes) of row r sits at r * 8 + (k ^ (r & 7)): conflict-free both when a
+    // thread writes its own row and when eight lanes read one row.
+    const int row_w = pos0 + t * kTileM + wq * 32;  // the warp's first row
+    const int k_rd = lane & 7;
+    if constexpr (DIRECT) {
+        // 64 output columns (128 bytes of bf16 / f16) per pass
 #pragma unroll
-    for (int c0 = 0; c0 < DV; c0 += 32) {
-        uint32_t o[32];
-        if (n_tiles > 0) ptx::tmem_ld_x32(tO + c0, o);
-        else {
+        for (int c0 = 0; c0 < DV; c0 += 64) {
+            uint32_t pk[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        if (row_ok) {
-            if constexpr (DIRECT) {
-                T *dst = (T *)out.ptr + row_offset(p, out, b, si.q0, pos) + (int64_t)h * out.sh + c0;
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t o[32];
+                if (n_tiles > 0) ptx::tmem_ld_x32(tO + c0 + 32 * hf, o);
+                else {
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    uint4 v;
-                    v.x = ptx::pack2(__uint_as_float(o[i + 0]) * inv, __uint_as_float(o[i + 1]) * inv, kBF16);
-                    v.y = ptx::pack2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv, kBF16);
-                    v.z = ptx::pack2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv, kBF16);
-                    v.w = ptx::pack2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv, kBF16);
-                    *(uint4 *)(dst + i) = v;
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[16 * hf + i] = ptx::pack2(__uint_as_float(o[2 * i]) * inv,
+                                                 __uint_as_float(o[2 * i + 1]) * inv, kBF16);
+            }
+            uint4 *st = reinterpret_cast<uint4 *>(stage);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                st[lane * 8 + (k ^ (lane & 7))] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = it * 4 + (lane >> 3);
+                if (row_w + r < si.sq) {
+                    T *dst = (T *)out.ptr + row_offset(p, out, b, si.q0, row_w + r) + (int64_t)h * out.sh +
+                             c0 + 8 * k_rd;
+                    *(uint4 *)dst = st[r * 8 + (k_rd ^ (r & 7))];
                 }
             }
+            __syncwarp();
         }
-        if constexpr (!DIRECT) {
-            // The warp's 32 rows x 32 columns go through its shared-memory slice, so that
-            // each store covers four whole 128-byte row segments instead of 16 bytes of 32
-            // rows. Slot k of row r sits at r * 8 + (k ^ (r & 7)): conflict-free both when
-            // a thread writes its row and when eight lanes read one row.
+    } else {
+        // 32 f32 partial columns (128 bytes) per pass
+#pragma unroll
+        for (int c0 = 0; c0 < DV; c0 += 32) {
+            uint32_t o[32];
+            if (n_tiles > 0) ptx::tmem_ld_x32(tO + c0, o);
+            else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 stage[lane * 8 + (k ^ (lane & 7))] =
                     make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
                                 __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
             __syncwarp();
-            const int k = lane & 7;
-            const int row_w = pos0 + t * kTileM + wq * 32;  // the warp's first row
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 const int r = it * 4 + (lane >> 3);
                 if (row_w + r < si.sq) {
                     float *dst = o_part + (((int64_t)h * p.S + s) * p.total_q + si.q0 + row_w + r) * DV +
-                                 c0 + 4 * k;
-                    *(float4 *)dst = stage[r * 8 + (k ^ (r & 7))];
+                                 c0 + 4 * k_rd;
+                    *(float4 *)dst = stage[r * 8 + (k_rd ^ (r & 7))];
                 }
             }
+            __syncwarp();
         }
-        __syncwarp();
     }
     if (row_ok) {
         if constexpr (DIRECT) {
