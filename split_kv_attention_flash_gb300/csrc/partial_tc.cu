@@ -60,17 +60,22 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchR
 // 5.6 TB/s of K and V here against 2.0 / 0.96 / 0.46 on the CUDA cores).
 constexpr int kMinQueries = 2;
 
-template <int DQK, int DV> struct Cfg {
+// KVI: M blocks of at most 128 rows. Tile 1 then holds no query of its own; instead it
+// takes the odd key tiles of tile 0's rows (tile 0 the even ones), into its own S / P / O
+// in TMEM, and the two halves are merged at the end. Only one Q tile is stored, which
+// leaves room for one more V stage at D_QK = 192 and 128.
+template <int DQK, int DV, bool KVI = false> struct Cfg {
+    static constexpr int kQTiles = KVI ? 1 : 2;
     static constexpr int kQBytes = kTileM * DQK * 2;
     static constexpr int kKBytes = kBN * DQK * 2;
     static constexpr int kVBytes = kBN * DV * 2;
     static constexpr int kKStages = DQK == 192 ? 2 : (DQK == 128 ? 3 : 4);
-    static constexpr int kVStages = DQK == 192 ? 1 : (DQK == 128 ? 2 : 4);
+    static constexpr int kVStages = DQK == 192 ? (KVI ? 2 : 1) : (DQK == 128 ? (KVI ? 3 : 2) : 4);
     // barriers: Q, K full/empty, V full/empty, S full x2, P full x2, O done x2, drain
     static constexpr int kBarQ = 0;
     static constexpr int kBarKF = 1;
     static constexpr int kBarKE = kBarKF + kKStages;
-    static constexpr bool kSplitV = kVStages == 1;          // V stage in two 64-key halves
+    static constexpr bool kSplitV = DQK == 192;             // V stages in two 64-key halves
     static constexpr int kVParts = kSplitV ? 2 : 1;
     static constexpr int kVPartBytes = kVBytes / kVParts;
     static constexpr int kVPanelBytes = kVPartBytes / (DV / 64);  // one 64-column panel of a part
@@ -81,7 +86,7 @@ template <int DQK, int DV> struct Cfg {
     static constexpr int kBarO = kBarP + 2;
     static constexpr int kBarDrain = kBarO + 2;
     static constexpr int kNumBars = kBarDrain + 1;
-    static constexpr int kTileBytes = 2 * kQBytes + kKStages * kKBytes + kVStages * kVBytes;
+    static constexpr int kTileBytes = kQTiles * kQBytes + kKStages * kKBytes + kVStages * kVBytes;
     static constexpr int kSmemBytes = 1024 + kTileBytes + kNumBars * 8 + 16;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "head dims");
@@ -190,12 +195,13 @@ __device__ __forceinline__ void merge_block(const Problem &p, const SeqInfo &si,
 // first (lpt_unit). Only instantiated for single-M-block launches (decode-like shapes with
 // a few queries per sequence), where ragged sequence lengths would otherwise leave the
 // longest sequences for the last wave; prefill launches keep the unit from blockIdx.
-template <typename T, int DQK, int DV, bool DIRECT, bool LPT = false>
+template <typename T, int DQK, int DV, bool DIRECT, bool LPT = false, bool KVI = false>
 __global__ void __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, Problem p, float *o_part,
                       float *lse_part, TensorView out, float *lse_out, int *tickets) {
-    using C = Cfg<DQK, DV>;
+    using C = Cfg<DQK, DV, KVI>;
+    static_assert(!KVI || (!DIRECT && LPT), "KVI is instantiated for partial launches of single M blocks");
     constexpr bool kBF16 = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
 
@@ -234,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
     const uint32_t sQ = (raw_u32 + 1023u) & ~1023u;
-    const uint32_t sK = sQ + 2 * C::kQBytes;
+    const uint32_t sK = sQ + C::kQTiles * C::kQBytes;
     const uint32_t sV = sK + C::kKStages * C::kKBytes;
     const uint32_t bar0 = sV + C::kVStages * C::kVBytes;
     uint8_t *const gen_base = smem_raw + (sQ - raw_u32);
@@ -289,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::prefetch_tensormap(&tmQ);
                 ptx::prefetch_tensormap(&tmK);
                 const int qrow = dense ? pos0 : si.q0 + pos0;
-                ptx::mbar_arrive_expect_tx(bar(C::kBarQ), 2 * C::kQBytes);
-                for (int t = 0; t < 2; ++t)
+                ptx::mbar_arrive_expect_tx(bar(C::kBarQ), C::kQTiles * C::kQBytes);
+                for (int t = 0; t < C::kQTiles; ++t)
                     for (int c = 0; c < DQK / 64; ++c)
                         ptx::tma_load_4d(sQ + t * C::kQBytes + c * kChunkBytes, &tmQ, bar(C::kBarQ),
                                          c * 64, qrow + t * kTileM, h, cb);
@@ -376,51 +382,126 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = ptx::mbar_wait_bounded(bar(C::kBarQ), 0, abort_flag, p.err, kErrMma, kTimeoutNs) &&
-                      ptx::mbar_wait_bounded(bar(C::kBarKF), 0, abort_flag, p.err, kErrMma, kTimeoutNs);
-            if (ok) {
-                ptx::tc_fence_after();
-                issue_qk(0, 0);
-                issue_qk(1, 0);
-                ptx::tc_commit(bar(C::kBarKE));
-            }
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int vs = j % C::kVStages;
-                const int kn = (j + 1) % C::kKStages;
-                const uint32_t vpar = (j / C::kVStages) & 1;
-                ok = ptx::mbar_wait_bounded(bar(C::kBarP + 0), j & 1, abort_flag, p.err, kErrMma,
-                                            kTimeoutNs);
-                for (int hf = 0; hf < C::kVParts && ok; ++hf) {
-                    ok = ptx::mbar_wait_bounded(bar(C::kBarVF + C::kVParts * vs + hf), vpar, abort_flag,
-                                                p.err, kErrMma, kTimeoutNs);
+            if constexpr (KVI) {
+                // tile t takes the key tiles k = 2 i + t: S_t(i) = Q0 K(k)^T, then
+                // O_t (+)= P_t(i) V(k); the order S0 S1 | PV0 S0 | PV1 S1 | ... is kept
+                auto wait_k = [&](int k) {
+                    return ptx::mbar_wait_bounded(bar(C::kBarKF + k % C::kKStages), (k / C::kKStages) & 1,
+                                                  abort_flag, p.err, kErrMma, kTimeoutNs);
+                };
+                auto issue_qk_k = [&](int t, int k) {
+                    const uint32_t kbase = sK + (k % C::kKStages) * C::kKBytes;
+#pragma unroll
+                    for (int kk = 0; kk < DQK / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                        ptx::mma_ss(tS[t], ptx::smem_desc_sw128(sQ + off, 16, 1024),
+                                    ptx::smem_desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0);
+                    }
+                    ptx::tc_commit(bar(C::kBarS + t));
+                    ptx::tc_commit(bar(C::kBarKE + k % C::kKStages));  // only S_t(i) reads K(k)
+                };
+                // V(k) part by part, each part freed once its MMAs are done
+                auto issue_pv_k = [&](int t, int k, int i) {
+                    constexpr int kSteps = kBN / 16 / C::kVParts;
+                    const int vs = k % C::kVStages;
+                    const uint32_t vpar = (k / C::kVStages) & 1;
+                    for (int hf = 0; hf < C::kVParts; ++hf) {
+                        if (!ptx::mbar_wait_bounded(bar(C::kBarVF + C::kVParts * vs + hf), vpar, abort_flag,
+                                                    p.err, kErrMma, kTimeoutNs))
+                            return false;
+                        ptx::tc_fence_after();
+                        const uint32_t vbase = sV + vs * C::kVBytes + hf * C::kVPartBytes;
+#pragma unroll
+                        for (int k4 = 0; k4 < kSteps; ++k4) {
+                            const int kk = hf * kSteps + k4;
+                            ptx::mma_ts(tO[t], tS[t] + kk * 8,
+                                        ptx::smem_desc_sw128(vbase + k4 * 2048, C::kVPanelBytes, 1024),
+                                        kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        ptx::tc_commit(bar(C::kBarVE + C::kVParts * vs + hf));
+                    }
+                    return true;
+                };
+                bool ok = ptx::mbar_wait_bounded(bar(C::kBarQ), 0, abort_flag, p.err, kErrMma, kTimeoutNs) &&
+                          wait_k(0);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_qk_k(0, 0);
+                }
+                if (ok && n_tiles > 1) {
+                    ok = wait_k(1);
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        issue_qk_k(1, 1);
+                    }
+                }
+                for (int i = 0; 2 * i < n_tiles && ok; ++i) {
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        const int k = 2 * i + t;
+                        if (k >= n_tiles) break;
+                        ok = ptx::mbar_wait_bounded(bar(C::kBarP + t), i & 1, abort_flag, p.err, kErrMma,
+                                                    kTimeoutNs) &&
+                             issue_pv_k(t, k, i);
+                        if (ok && k + 2 < n_tiles) {
+                            ok = wait_k(k + 2);
+                            if (ok) {
+                                ptx::tc_fence_after();
+                                issue_qk_k(t, k + 2);
+                            }
+                        }
+                    }
+                }
+                if (ok) {
+                    ptx::tc_commit(bar(C::kBarO + 0));
+                    ptx::tc_commit(bar(C::kBarO + 1));
+                }
+            } else {
+                bool ok = ptx::mbar_wait_bounded(bar(C::kBarQ), 0, abort_flag, p.err, kErrMma, kTimeoutNs) &&
+                          ptx::mbar_wait_bounded(bar(C::kBarKF), 0, abort_flag, p.err, kErrMma, kTimeoutNs);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_qk(0, 0);
+                    issue_qk(1, 0);
+                    ptx::tc_commit(bar(C::kBarKE));
+                }
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    const int vs = j % C::kVStages;
+                    const int kn = (j + 1) % C::kKStages;
+                    const uint32_t vpar = (j / C::kVStages) & 1;
+                    ok = ptx::mbar_wait_bounded(bar(C::kBarP + 0), j & 1, abort_flag, p.err, kErrMma,
+                                                kTimeoutNs);
+                    for (int hf = 0; hf < C::kVParts && ok; ++hf) {
+                        ok = ptx::mbar_wait_bounded(bar(C::kBarVF + C::kVParts * vs + hf), vpar, abort_flag,
+                                                    p.err, kErrMma, kTimeoutNs);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_pv_part(0, j, hf);
+                    }
+                    if (!ok) break;
+                    if (j + 1 < n_tiles) {
+                        ok = ptx::mbar_wait_bounded(bar(C::kBarKF + kn), ((j + 1) / C::kKStages) & 1,
+                                                    abort_flag, p.err, kErrMma, kTimeoutNs);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        issue_qk(0, j + 1);
+                    }
+                    ok = ptx::mbar_wait_bounded(bar(C::kBarP + 1), j & 1, abort_flag, p.err, kErrMma,
+                                                kTimeoutNs);
                     if (!ok) break;
                     ptx::tc_fence_after();
-                    issue_pv_part(0, j, hf);
+                    for (int hf = 0; hf < C::kVParts; ++hf) {
+                        issue_pv_part(1, j, hf);
+                        ptx::tc_commit(bar(C::kBarVE + C::kVParts * vs + hf));  // this part of V(j) is free
+                    }
+                    if (j + 1 < n_tiles) {
+                        issue_qk(1, j + 1);
+                        ptx::tc_commit(bar(C::kBarKE + kn));
+                    }
                 }
-                if (!ok) break;
-                if (j + 1 < n_tiles) {
-                    ok = ptx::mbar_wait_bounded(bar(C::kBarKF + kn), ((j + 1) / C::kKStages) & 1,
-                                                abort_flag, p.err, kErrMma, kTimeoutNs);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    issue_qk(0, j + 1);
+                if (ok) {
+                    ptx::tc_commit(bar(C::kBarO + 0));
+                    ptx::tc_commit(bar(C::kBarO + 1));
                 }
-                ok = ptx::mbar_wait_bounded(bar(C::kBarP + 1), j & 1, abort_flag, p.err, kErrMma,
-                                            kTimeoutNs);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                for (int hf = 0; hf < C::kVParts; ++hf) {
-                    issue_pv_part(1, j, hf);
-                    ptx::tc_commit(bar(C::kBarVE + C::kVParts * vs + hf));  // this part of V(j) is free
-                }
-                if (j + 1 < n_tiles) {
-                    issue_qk(1, j + 1);
-                    ptx::tc_commit(bar(C::kBarKE + kn));
-                }
-            }
-            if (ok) {
-                ptx::tc_commit(bar(C::kBarO + 0));
-                ptx::tc_commit(bar(C::kBarO + 1));
             }
             // every issued MMA must be finished before TMEM is released
             int dummy = 0;
@@ -437,9 +518,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue staging: 4 KB per softmax warp in the K stages, which no load or MMA
         // touches once the O-done barrier has completed (or when the split has no tile)
         float4 *stage = (float4 *)(gen_base + (sK - sQ)) + warp * 256;
-        softmax_rows<T, DV, DIRECT>(p, si, b, h, s, pos0, t, tmem, kb, ke, n_tiles, sb,
-                                           abort_flag, o_part, lse_part, out, lse_out, stage);
-        if constexpr (!DIRECT) {
+        if constexpr (KVI) {
+            // the two halves swap m and l through the Q tile's memory: every MMA has
+            // finished once the O-done barrier completed (or no load was issued at all)
+            float m_r = -INFINITY, l_r = 0.f;
+            const bool ok_r = softmax_rows<T, DV, false, true>(p, si, b, h, s, pos0, t, tmem, kb, ke, n_tiles,
+                                                              sb, abort_flag, o_part, lse_part, out, lse_out,
+                                                              stage, &m_r, &l_r);
+            kvi_epilogue<DV>(p, si, h, s, pos0, t, tmem, n_tiles, m_r, l_r, ok_r, (float *)gen_base, stage,
+                             o_part, lse_part);
+        } else {
+            softmax_rows<T, DV, DIRECT>(p, si, b, h, s, pos0, t, tmem, kb, ke, n_tiles, sb,
+                                        abort_flag, o_part, lse_part, out, lse_out, stage);
+        }
+        if constexpr (!DIRECT && !KVI) {
             // Fused merge: the CTA of this (sequence, head, M block) that writes its
             // partials last merges all splits. Every softmax thread takes part in both
             // barriers, also after an abort. Shared memory is free by now: every MMA and
@@ -513,12 +605,12 @@ bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long long r
     return r == CUDA_SUCCESS;
 }
 
-template <typename T, int DQK, int DV, bool DIRECT, bool LPT = false>
+template <typename T, int DQK, int DV, bool DIRECT, bool LPT = false, bool KVI = false>
 static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                               const CUtensorMap &mv, float *o_part, float *lse_part,
                               const TensorView &out, float *lse_out, int *tickets, cudaStream_t st) {
-    using C = Cfg<DQK, DV>;
-    auto kern = partial_tc_kernel<T, DQK, DV, DIRECT, LPT>;
+    using C = Cfg<DQK, DV, KVI>;
+    auto kern = partial_tc_kernel<T, DQK, DV, DIRECT, LPT, KVI>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -542,9 +634,13 @@ static cudaError_t launch_dims(const Problem &p, const CUtensorMap &mq, const CU
     if (out && !tickets)
         return launch_cfg<T, DQK, DV, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out, nullptr, st);
     const long long units = (long long)p.B * p.S;
-    if (!(out && tickets) && p.max_sq <= kBM && units > 1 && units <= kLptMaxUnits)
+    if (!(out && tickets) && p.max_sq <= kBM && units > 1 && units <= kLptMaxUnits) {
+        if (p.max_sq <= kTileM)
+            return launch_cfg<T, DQK, DV, false, true, true>(p, mq, mk, mv, o_part, lse_part, TensorView{},
+                                                             nullptr, nullptr, st);
         return launch_cfg<T, DQK, DV, false, true>(p, mq, mk, mv, o_part, lse_part, TensorView{}, nullptr,
                                                    nullptr, st);
+    }
     return launch_cfg<T, DQK, DV, false>(p, mq, mk, mv, o_part, lse_part, out ? *out : TensorView{},
                                          out ? lse_out : nullptr, out ? tickets : nullptr, st);
 }

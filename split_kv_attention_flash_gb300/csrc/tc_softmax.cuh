@@ -68,18 +68,22 @@ struct SoftmaxBars {
 //     warp-collective; S_t(j) completing implies PV_t(j - 1) did, so O_t is stable),
 //   * p = 2^(s * scale * log2 e - m) written back as 16-bit pairs over S's first
 //     64 columns, then P_t(j) is reported.
+// KVI (M blocks of at most 128 rows): both warpgroups own the same 128 rows, and tile t
+// takes the key tiles 2 i + t; the loop then hands back its m and l (base 2) instead of
+// writing anything, and kvi_epilogue merges the two halves.
 // Returns false when a wait gave up (the CTA's abort flag is then raised).
-template <typename T, int DV, bool DIRECT>
+template <typename T, int DV, bool DIRECT, bool KVI = false>
 __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si, int b, int h, int s,
                                              int pos0, int t, uint32_t tmem, int kb, int ke,
                                              int n_tiles, const SoftmaxBars &bars,
                                              volatile int *abort_flag, float *o_part,
                                              float *lse_part, const TensorView &out, float *lse_out,
-                                             float4 *stage) {
+                                             float4 *stage, float *m_out = nullptr,
+                                             float *l_out = nullptr) {
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3;
-    const int pos = pos0 + t * kTileM + wq * 32 + lane;
+    const int pos = pos0 + (KVI ? 0 : t * kTileM) + wq * 32 + lane;
     const bool row_ok = pos < si.sq;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)t * 128u;
@@ -92,14 +96,16 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    const int n_mine = KVI ? (n_tiles + 1 - t) / 2 : n_tiles;  // KVI: t = 0 even, t = 1 odd tiles
+    for (int j = 0; j < n_mine; ++j) {
         ok = warp_wait(bars.s_full, j & 1, abort_flag, p.err, kErrSoftmax);
         if (!ok) break;
         ptx::tc_fence_after();
         uint32_t r[128];
         ptx::tmem_ld_x128(tS, r);
-        const int nvalid = kend - (kb + j * kBN);
-        const int nlow = kfirst - (kb + j * kBN);
+        const int kt = KVI ? 2 * j + t : j;  // the key tile
+        const int nvalid = kend - (kb + kt * kBN);
+        const int nlow = kfirst - (kb + kt * kBN);
         if (nvalid < kBN || nlow > 0) {
 #pragma unroll
             for (int c = 0; c < 128; ++c)
@@ -156,6 +162,11 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
         ptx::mbar_arrive(bars.p_ready);
     }
     if (ok && n_tiles > 0) ok = warp_wait(bars.o_done, 0, abort_flag, p.err, kErrSoftmax);
+    if constexpr (KVI) {
+        *m_out = m;
+        *l_out = l;
+        return ok;
+    }
     if (!ok) return false;
     ptx::tc_fence_after();
     const bool empty = !(l > 0.f);
@@ -238,6 +249,79 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
         }
     }
     return true;
+}
+
+// The KVI merge of the two halves of a 128-row M block. Warpgroup t held
+// (m_t, l_t, O_t) over the key tiles 2 i + t (O_t in TMEM columns 256 + 128 t, scaled by
+// 2^-m_t); with M = max(m_0, m_1) and a_t = 2^(m_t - M) (0 where l_t = 0):
+//   O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1),  L = ln 2 * (M + log2(a_0 l_0 + a_1 l_1))
+// -- the merge of two splits, inside the CTA. The warpgroups swap m and l through shared
+// memory (`xchg`, 2 KB that no load or MMA touches any more), then warpgroup t writes
+// output columns [t DV / 2, (t + 1) DV / 2) through its warps' staging slices, and
+// warpgroup 0 the LSE. Every softmax thread reaches the barrier, also after an abort.
+template <int DV>
+__device__ __forceinline__ void kvi_epilogue(const Problem &p, const SeqInfo &si, int h, int s,
+                                             int pos0, int t, uint32_t tmem, int n_tiles, float m,
+                                             float l, bool ok, float *xchg, float4 *stage,
+                                             float *o_part, float *lse_part) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wq = warp & 3;
+    const int i = wq * 32 + lane;
+    if (ok) {
+        xchg[(2 * t) * kTileM + i] = m;
+        xchg[(2 * t + 1) * kTileM + i] = l;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (!ok) return;  // warp-uniform
+    const float mo = xchg[(2 * (1 - t)) * kTileM + i], lo = xchg[(2 * (1 - t) + 1) * kTileM + i];
+    const float m0 = t == 0 ? m : mo, l0 = t == 0 ? l : lo;
+    const float m1 = t == 0 ? mo : m, l1 = t == 0 ? lo : l;
+    const float mx = fmaxf(m0, m1);
+    const float a0 = l0 > 0.f ? ptx::ex2(m0 - mx) : 0.f;
+    const float a1 = l1 > 0.f ? ptx::ex2(m1 - mx) : 0.f;
+    const float sum = a0 * l0 + a1 * l1;
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    const float w0 = a0 * inv, w1 = a1 * inv;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const int row_w = pos0 + wq * 32;  // the warp's first row
+    const int k_rd = lane & 7;
+#pragma unroll
+    for (int c0 = t * (DV / 2); c0 < (t + 1) * (DV / 2); c0 += 32) {
+        uint32_t o0[32], o1[32];
+        if (n_tiles > 0) ptx::tmem_ld_x32(tmem + lane_off + 256u + c0, o0);
+        else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o0[c] = 0u;
+        }
+        if (n_tiles > 1) ptx::tmem_ld_x32(tmem + lane_off + 384u + c0, o1);
+        else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o1[c] = 0u;
+        }
+        // slot k of row r at r * 8 + (k ^ (r & 7)), as in softmax_rows
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = w0 * __uint_as_float(o0[4 * k + u]) + w1 * __uint_as_float(o1[4 * k + u]);
+            stage[lane * 8 + (k ^ (lane & 7))] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int r = it * 4 + (lane >> 3);
+            if (row_w + r < si.sq) {
+                float *dst = o_part + (((int64_t)h * p.S + s) * p.total_q + si.q0 + row_w + r) * DV +
+                             c0 + 4 * k_rd;
+                *(float4 *)dst = stage[r * 8 + (k_rd ^ (r & 7))];
+            }
+        }
+        __syncwarp();
+    }
+    if (t == 0 && pos0 + i < si.sq)
+        lse_part[((int64_t)h * p.S + s) * p.total_q + si.q0 + pos0 + i] =
+            sum > 0.f ? (mx + log2f(sum)) * 0.69314718055994530942f : -INFINITY;
 }
 
 }  // namespace tc

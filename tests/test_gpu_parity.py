@@ -57,11 +57,21 @@ SMALL = [
     _small("bf16", 64, 64, mask=wl.MASK_PREFIX_CAUSAL, po=2000, S=6, bn=128, window=700,
            sq=(1, 3, 16), sk=(3000, 2500, 2100)),
     _small("f32", 128, 128, mask=wl.MASK_CAUSAL, S=3, bn=32, window=40, used=(800, 5, 0, 300)),
-    # unmasked, two or more M blocks: CTA pairs sharing each MMA, including pairs whose
-    # second block lies past its sequence, padded key slots, lastValid and S = 1
+    # unmasked, two or more M blocks, including blocks past a sequence's end, padded key
+    # slots and lastValid
     _small("f16", 192, 128, S=2, bn=128, sq=(600, 257, 3), sk=(900, 1300, 40)),
     _small("bf16", 192, 128, S=3, bn=128, sq=(520, 300), sk=(2000, 700), used=(1800, 1)),
     _small("f16", 128, 128, lvi=600, S=4, bn=64, sq=(700,), sk=(1500,)),
+    # at most 128 queries per sequence: the tensor-core kernel splits each block's key
+    # tiles between its two halves (odd and even tile counts, one-tile splits, masks,
+    # windows, padded key slots, each head dim)
+    _small("bf16", 192, 128, mask=wl.MASK_PREFIX_CAUSAL, po=1000, S=3, bn=128,
+           sq=(128, 100, 2, 77), sk=(3000, 1500, 700, 129)),
+    _small("f16", 128, 128, lvi=900, S=4, bn=64, sq=(64, 128, 5), sk=(2000, 900, 3000)),
+    _small("bf16", 128, 128, mask=wl.MASK_PREFIX_CAUSAL, po=1500, S=2, bn=128, window=300,
+           sq=(120, 128), sk=(2000, 1700), used=(1900, 1650)),
+    _small("bf16", 64, 64, S=5, bn=128, sq=(33, 2), sk=(5000, 4000)),
+    # S = 1 writes the output directly
     _small("bf16", 192, 128, S=1, bn=128, sq=(513, 40), sk=(1000, 3000)),
 ]
 
