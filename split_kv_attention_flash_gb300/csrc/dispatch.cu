@@ -3,11 +3,11 @@
 
 namespace sk {
 
-// Tensor cores (tcgen05) for 16-bit storage with the library's M block and at least
-// two queries in the longest sequence; the streaming decode kernel for 16-bit storage
-// with one query per sequence (and up to 16 when the tensor-core kernel does not
-// apply); the CUDA-core kernel for the rest
-// (f32 storage, other M blocks, no keys, tensors TMA cannot describe).
+// Tensor cores (tcgen05) for 16-bit storage with the library's M block, except one query
+// per sequence with more than 256 (sequence, split) units; the streaming decode kernel
+// for those (and for up to 16 queries when the tensor-core kernel does not apply); the
+// CUDA-core kernel for the rest (f32 storage, other M blocks, no keys, tensors TMA cannot
+// describe).
 const char *partial_kernel_name(const Problem &p, int dtype, const TensorView &q,
                                 const TensorView &k, const TensorView &v) {
     (void)q; (void)k; (void)v;

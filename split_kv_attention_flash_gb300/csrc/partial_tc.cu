@@ -55,10 +55,12 @@ constexpr int kSoftmaxRegs = 208;
 constexpr int kControlRegs = 88;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch budget");
-// Sequences of one query go to the CUDA-core decode kernel; from two queries on the
-// tensor cores stream K and V faster (B32 H32 D128, 4 / 8 / 16 queries: 5.8 / 5.6 /
-// 5.6 TB/s of K and V here against 2.0 / 0.96 / 0.46 on the CUDA cores).
-constexpr int kMinQueries = 2;
+// Launches whose M blocks hold at most 128 queries split each block's key tiles between
+// the two halves (KVI); that instantiation also takes its (sequence, split) units longest
+// first, which needs at most kLptMaxUnits of them. One query per sequence comes here only
+// in that case (B32 H32 D128 decode: 5.2 ms here against 6.5 ms on the streaming decode
+// kernel); with more units it stays on the decode kernel, where the two-tile form here
+// was slower.
 
 // KVI: M blocks of at most 128 rows. Tile 1 then holds no query of its own; instead it
 // takes the odd key tiles of tile 0's rows (tile 0 the even ones), into its own S / P / O
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmV, Problem p, float *o_part,
                       float *lse_part, TensorView out, float *lse_out, int *tickets) {
     using C = Cfg<DQK, DV, KVI>;
-    static_assert(!KVI || (!DIRECT && LPT), "KVI is instantiated for partial launches of single M blocks");
+    static_assert(!KVI || LPT, "KVI is instantiated for single-M-block launches");
     constexpr bool kBF16 = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
 
@@ -525,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool ok_r = softmax_rows<T, DV, false, true>(p, si, b, h, s, pos0, t, tmem, kb, ke, n_tiles,
                                                               sb, abort_flag, o_part, lse_part, out, lse_out,
                                                               stage, &m_r, &l_r);
-            kvi_epilogue<DV>(p, si, h, s, pos0, t, tmem, n_tiles, m_r, l_r, ok_r, (float *)gen_base, stage,
-                             o_part, lse_part);
+            kvi_epilogue<T, DV, DIRECT>(p, si, b, h, s, pos0, t, tmem, n_tiles, m_r, l_r, ok_r,
+                                        (float *)gen_base, stage, o_part, lse_part, out, lse_out);
         } else {
             softmax_rows<T, DV, DIRECT>(p, si, b, h, s, pos0, t, tmem, kb, ke, n_tiles, sb,
                                         abort_flag, o_part, lse_part, out, lse_out, stage);
@@ -631,16 +633,21 @@ template <typename T, int DQK, int DV>
 static cudaError_t launch_dims(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                const CUtensorMap &mv, float *o_part, float *lse_part,
                                const TensorView *out, float *lse_out, int *tickets, cudaStream_t st) {
-    if (out && !tickets)
-        return launch_cfg<T, DQK, DV, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out, nullptr, st);
     const long long units = (long long)p.B * p.S;
-    if (!(out && tickets) && p.max_sq <= kBM && units > 1 && units <= kLptMaxUnits) {
-        if (p.max_sq <= kTileM)
-            return launch_cfg<T, DQK, DV, false, true, true>(p, mq, mk, mv, o_part, lse_part, TensorView{},
-                                                             nullptr, nullptr, st);
+    if (out && !tickets) {
+        // S == 1: the output is written directly
+        if (p.max_sq <= kTileM && units <= kLptMaxUnits)
+            return launch_cfg<T, DQK, DV, true, true, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out,
+                                                            nullptr, st);
+        return launch_cfg<T, DQK, DV, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out, nullptr, st);
+    }
+    // partials only (no fused merge): single-M-block launches take their units longest first
+    if (!(out && tickets) && p.max_sq <= kTileM && units <= kLptMaxUnits)
+        return launch_cfg<T, DQK, DV, false, true, true>(p, mq, mk, mv, o_part, lse_part, TensorView{},
+                                                         nullptr, nullptr, st);
+    if (!(out && tickets) && p.max_sq <= kBM && units > 1 && units <= kLptMaxUnits)
         return launch_cfg<T, DQK, DV, false, true>(p, mq, mk, mv, o_part, lse_part, TensorView{}, nullptr,
                                                    nullptr, st);
-    }
     return launch_cfg<T, DQK, DV, false>(p, mq, mk, mv, o_part, lse_part, out ? *out : TensorView{},
                                          out ? lse_out : nullptr, out ? tickets : nullptr, st);
 }
@@ -651,7 +658,8 @@ bool partial_tc_supported(const Problem &p, int dtype) {
           (p.d_qk == 192 && p.d_v == 128)))
         return false;
     if (p.bm != kBM || p.total_k <= 0 || p.max_sk <= 0 || p.total_q <= 0) return false;
-    if (p.max_sq < kMinQueries) return false;
+    if (p.max_sq < 1) return false;
+    if (p.max_sq == 1 && (long long)p.B * p.S > kLptMaxUnits) return false;
     if ((long long)p.B * p.S > 65535 || p.H > 65535) return false;
     if (encode_fn() == nullptr) return false;
     return true;

@@ -256,14 +256,19 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
 // 2^-m_t); with M = max(m_0, m_1) and a_t = 2^(m_t - M) (0 where l_t = 0):
 //   O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1),  L = ln 2 * (M + log2(a_0 l_0 + a_1 l_1))
 // -- the merge of two splits, inside the CTA. The warpgroups swap m and l through shared
-// memory (`xchg`, 2 KB that no load or MMA touches any more), then warpgroup t writes
-// output columns [t DV / 2, (t + 1) DV / 2) through its warps' staging slices, and
-// warpgroup 0 the LSE. Every softmax thread reaches the barrier, also after an abort.
-template <int DV>
-__device__ __forceinline__ void kvi_epilogue(const Problem &p, const SeqInfo &si, int h, int s,
+// memory (`xchg`, 2 KB that no load or MMA touches any more); then each warpgroup writes
+// its share of the columns (the f32 partial O_s, or with DIRECT the output itself)
+// through its warps' staging slices, 128 bytes of a row per pass, and warpgroup 0 the
+// LSE. Every softmax thread reaches the barrier, also after an abort.
+template <typename T, int DV, bool DIRECT>
+__device__ __forceinline__ void kvi_epilogue(const Problem &p, const SeqInfo &si, int b, int h, int s,
                                              int pos0, int t, uint32_t tmem, int n_tiles, float m,
                                              float l, bool ok, float *xchg, float4 *stage,
-                                             float *o_part, float *lse_part) {
+                                             float *o_part, float *lse_part, const TensorView &out,
+                                             float *lse_out) {
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int kPassCols = DIRECT ? 64 : 32;                        // 128 bytes of a row
+    constexpr int kMyCols = DV / 2 >= kPassCols ? DV / 2 : kPassCols;  // columns per warpgroup
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3;
     const int i = wq * 32 + lane;
@@ -285,8 +290,8 @@ __device__ __forceinline__ void kvi_epilogue(const Problem &p, const SeqInfo &si
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int row_w = pos0 + wq * 32;  // the warp's first row
     const int k_rd = lane & 7;
-#pragma unroll
-    for (int c0 = t * (DV / 2); c0 < (t + 1) * (DV / 2); c0 += 32) {
+    // 32 merged columns c0 .. c0 + 31 of this thread's row
+    auto merged = [&](int c0, float (&v)[32]) {
         uint32_t o0[32], o1[32];
         if (n_tiles > 0) ptx::tmem_ld_x32(tmem + lane_off + 256u + c0, o0);
         else {
@@ -298,30 +303,62 @@ __device__ __forceinline__ void kvi_epilogue(const Problem &p, const SeqInfo &si
 #pragma unroll
             for (int c = 0; c < 32; ++c) o1[c] = 0u;
         }
-        // slot k of row r at r * 8 + (k ^ (r & 7)), as in softmax_rows
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float v[4];
+        for (int c = 0; c < 32; ++c) v[c] = w0 * __uint_as_float(o0[c]) + w1 * __uint_as_float(o1[c]);
+    };
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                v[u] = w0 * __uint_as_float(o0[4 * k + u]) + w1 * __uint_as_float(o1[4 * k + u]);
-            stage[lane * 8 + (k ^ (lane & 7))] = make_float4(v[0], v[1], v[2], v[3]);
-        }
-        __syncwarp();
+    for (int c0 = t * kMyCols; c0 < DV && c0 < (t + 1) * kMyCols; c0 += kPassCols) {
+        // slot k (16 bytes) of row r at r * 8 + (k ^ (r & 7)), as in softmax_rows
+        if constexpr (DIRECT) {
+            uint4 *st = reinterpret_cast<uint4 *>(stage);
+            uint32_t pk[32];
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int r = it * 4 + (lane >> 3);
-            if (row_w + r < si.sq) {
-                float *dst = o_part + (((int64_t)h * p.S + s) * p.total_q + si.q0 + row_w + r) * DV +
-                             c0 + 4 * k_rd;
-                *(float4 *)dst = stage[r * 8 + (k_rd ^ (r & 7))];
+            for (int hf = 0; hf < 2; ++hf) {
+                float v[32];
+                merged(c0 + 32 * hf, v);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) pk[16 * hf + c] = ptx::pack2(v[2 * c], v[2 * c + 1], kBF16);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                st[lane * 8 + (k ^ (lane & 7))] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = it * 4 + (lane >> 3);
+                if (row_w + r < si.sq) {
+                    T *dst = (T *)out.ptr + row_offset(p, out, b, si.q0, row_w + r) + (int64_t)h * out.sh +
+                             c0 + 8 * k_rd;
+                    *(uint4 *)dst = st[r * 8 + (k_rd ^ (r & 7))];
+                }
+            }
+        } else {
+            float v[32];
+            merged(c0, v);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                stage[lane * 8 + (k ^ (lane & 7))] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int r = it * 4 + (lane >> 3);
+                if (row_w + r < si.sq) {
+                    float *dst = o_part + (((int64_t)h * p.S + s) * p.total_q + si.q0 + row_w + r) * DV +
+                                 c0 + 4 * k_rd;
+                    *(float4 *)dst = stage[r * 8 + (k_rd ^ (r & 7))];
+                }
             }
         }
         __syncwarp();
     }
-    if (t == 0 && pos0 + i < si.sq)
-        lse_part[((int64_t)h * p.S + s) * p.total_q + si.q0 + pos0 + i] =
-            sum > 0.f ? (mx + log2f(sum)) * 0.69314718055994530942f : -INFINITY;
+    if (t == 0 && pos0 + i < si.sq) {
+        const float lse = sum > 0.f ? (mx + log2f(sum)) * 0.69314718055994530942f : -INFINITY;
+        if constexpr (DIRECT) {
+            if (lse_out) lse_out[(int64_t)h * p.total_q + si.q0 + pos0 + i] = lse;
+        } else {
+            lse_part[((int64_t)h * p.S + s) * p.total_q + si.q0 + pos0 + i] = lse;
+        }
+    }
 }
 
 }  // namespace tc

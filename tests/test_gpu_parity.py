@@ -211,6 +211,27 @@ def test_decode_kernel_with_several_queries(dtype, mask, po):
     H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
 
 
+@pytest.mark.parametrize("B,S,kernel", [(8, 4, "partial_tc"), (64, 4, "partial_tc"),
+                                         (65, 4, "partial_decode"), (130, 2, "partial_decode")])
+def test_single_query_routes_by_unit_count(B, S, kernel):
+    """One query per sequence runs on the tensor-core kernel while the (sequence, split)
+    units number at most 256, on the streaming decode kernel beyond; both match the oracle."""
+    rng = np.random.default_rng(B)
+    w = _small("bf16", 128, 128, S=S, bn=128, sq=(1,) * B,
+               sk=tuple(int(x) for x in rng.integers(0, 700, B)))
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    p = skv.params_for(w, DEV, split_kv=S)
+    assert skv.sk_partial_kernel_name(p, qd, kd, vd) == kernel
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    for split in (S, 1):
+        out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV, split_kv=split)
+        H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, f"forward S={split}")
+    o_part, l_part, _ = H.run_partials(w, qd, kd, vd, DEV, S)
+    ref_po, ref_pl = oracle.partials(H.oracle_problem(w, S), q, k, v)
+    H.assert_close(o_part.permute(2, 0, 1, 3).cpu().numpy(), l_part.permute(2, 0, 1).cpu().numpy(),
+                   ref_po, ref_pl, w.dtype, "partials")
+
+
 def test_long_single_sequence_sampled():
     """One sequence of 262144 keys (well past the workloads' longest), sampled rows."""
     w = wl.Workload("long single sequence", H=2, seqlens_q=(512,), seqlens_k=(262144,), d_qk=128,
