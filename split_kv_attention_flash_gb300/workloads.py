@@ -154,7 +154,7 @@ WINDOW = TARGET_SHAPE.with_(name="sliding-window prefill bf16 Sq4096 Sk42700 H12
 DECODE_MQ = DECODE.with_(name="multi-query decode bf16 (B32 H32 Sq8, Sk ~ U[4096, 131072], D128)",
                          seqlens_q=(8,) * 32)
 
-# a 2 GB decode case with the decode workload's layout (for profiler captures)
+# a 4.3 GB decode case with the decode workload's layout (for profiler captures)
 DECODE_SMALL = DECODE.with_(name="decode bf16 (B32 H32 Sq1, Sk 8192, D128)", seqlens_k=(8192,) * 32)
 
 ALL = {"decode_small": DECODE_SMALL, "decode_mq": DECODE_MQ, "window": WINDOW, "tiny": TINY_CAUSAL, "noncausal": NONCAUSAL_BF16, "masked": MASKED_F16,
