@@ -3,11 +3,11 @@
 
 namespace sk {
 
-// Tensor cores (tcgen05) for 16-bit storage with the library's M block, except one query
-// per sequence with more than 256 (sequence, split) units; the streaming decode kernel
-// for those (and for up to 16 queries when the tensor-core kernel does not apply); the
-// CUDA-core kernel for the rest (f32 storage, other M blocks, no keys, tensors TMA cannot
-// describe).
+// Tensor cores (tcgen05) for 16-bit storage with the library's M block (prefill and decode);
+// the streaming decode kernel for up to 16 queries per sequence where the tensor-core
+// kernel does not apply (other M blocks, more than 65535 (sequence, split) units, tensors
+// its TMA maps cannot describe); the CUDA-core kernel for the rest (f32 storage, other M
+// blocks, no keys).
 const char *partial_kernel_name(const Problem &p, int dtype, const TensorView &q,
                                 const TensorView &k, const TensorView &v) {
     (void)q; (void)k; (void)v;

@@ -1,6 +1,6 @@
-// partial_decode.cu -- split partials for sequences of one query (decode) where the
-// tensor-core kernel's single-block form does not apply: more than 256 (sequence, split)
-// units, or an M block other than 256 rows (then up to 16 queries); bf16 / f16 storage.
+// partial_decode.cu -- split partials for sequences of up to 16 queries (decode) where the
+// tensor-core kernel does not apply: an M block other than its 256 rows, more than 65535
+// (sequence, split) units, or tensors its TMA maps cannot describe; bf16 / f16 storage.
 //
 // [P1] Summary / Technical details: O_s and L_s of one (sequence, head, split) over
 // the split's key run, empty splits giving O_s = 0 and L_s = -inf. With a handful

@@ -56,11 +56,10 @@ constexpr int kControlRegs = 88;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch budget");
 // Launches whose M blocks hold at most 128 queries split each block's key tiles between
-// the two halves (KVI); that instantiation also takes its (sequence, split) units longest
-// first, which needs at most kLptMaxUnits of them. One query per sequence comes here only
-// in that case (B32 H32 D128 decode: 5.2 ms here against 6.5 ms on the streaming decode
-// kernel); with more units it stays on the decode kernel, where the two-tile form here
-// was slower.
+// the two halves (KVI), taking their (sequence, split) units longest first when there are
+// at most kLptMaxUnits of them and in index order otherwise. One query per sequence comes
+// here too: B32 H32 D128 decode takes 5.2 ms (7.4 TB/s of K and V) against 6.5 ms on the
+// CUDA-core streaming decode kernel, 5.3-5.4 ms against 6.7-6.8 ms with 512-1024 units.
 
 // KVI: M blocks of at most 128 rows. Tile 1 then holds no query of its own; instead it
 // takes the odd key tiles of tile 0's rows (tile 0 the even ones), into its own S / P / O
@@ -203,7 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmV, Problem p, float *o_part,
                       float *lse_part, TensorView out, float *lse_out, int *tickets) {
     using C = Cfg<DQK, DV, KVI>;
-    static_assert(!KVI || LPT, "KVI is instantiated for single-M-block launches");
     constexpr bool kBF16 = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
 
@@ -639,12 +637,18 @@ static cudaError_t launch_dims(const Problem &p, const CUtensorMap &mq, const CU
         if (p.max_sq <= kTileM && units <= kLptMaxUnits)
             return launch_cfg<T, DQK, DV, true, true, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out,
                                                             nullptr, st);
+        if (p.max_sq <= kTileM)
+            return launch_cfg<T, DQK, DV, true, false, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out,
+                                                             nullptr, st);
         return launch_cfg<T, DQK, DV, true>(p, mq, mk, mv, o_part, lse_part, *out, lse_out, nullptr, st);
     }
     // partials only (no fused merge): single-M-block launches take their units longest first
     if (!(out && tickets) && p.max_sq <= kTileM && units <= kLptMaxUnits)
         return launch_cfg<T, DQK, DV, false, true, true>(p, mq, mk, mv, o_part, lse_part, TensorView{},
                                                          nullptr, nullptr, st);
+    if (!(out && tickets) && p.max_sq <= kTileM)  // too many units to rank: index order
+        return launch_cfg<T, DQK, DV, false, false, true>(p, mq, mk, mv, o_part, lse_part, TensorView{},
+                                                          nullptr, nullptr, st);
     if (!(out && tickets) && p.max_sq <= kBM && units > 1 && units <= kLptMaxUnits)
         return launch_cfg<T, DQK, DV, false, true>(p, mq, mk, mv, o_part, lse_part, TensorView{}, nullptr,
                                                    nullptr, st);
@@ -659,7 +663,6 @@ bool partial_tc_supported(const Problem &p, int dtype) {
         return false;
     if (p.bm != kBM || p.total_k <= 0 || p.max_sk <= 0 || p.total_q <= 0) return false;
     if (p.max_sq < 1) return false;
-    if (p.max_sq == 1 && (long long)p.B * p.S > kLptMaxUnits) return false;
     if ((long long)p.B * p.S > 65535 || p.H > 65535) return false;
     if (encode_fn() == nullptr) return false;
     return true;

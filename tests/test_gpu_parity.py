@@ -211,11 +211,12 @@ def test_decode_kernel_with_several_queries(dtype, mask, po):
     H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
 
 
-@pytest.mark.parametrize("B,S,kernel", [(8, 4, "partial_tc"), (64, 4, "partial_tc"),
-                                         (65, 4, "partial_decode"), (130, 2, "partial_decode")])
-def test_single_query_routes_by_unit_count(B, S, kernel):
-    """One query per sequence runs on the tensor-core kernel while the (sequence, split)
-    units number at most 256, on the streaming decode kernel beyond; both match the oracle."""
+@pytest.mark.parametrize("B,S", [(8, 4), (64, 4), (65, 4), (130, 2)])
+def test_single_query_on_the_tensor_cores(B, S):
+    """One query per sequence runs on the tensor-core kernel's single-block form: units taken
+    longest first up to 256 (sequence, split) units, in index order beyond; both match the
+    oracle, for the partials and for the output written directly at split 1."""
+    kernel = "partial_tc"
     rng = np.random.default_rng(B)
     w = _small("bf16", 128, 128, S=S, bn=128, sq=(1,) * B,
                sk=tuple(int(x) for x in rng.integers(0, 700, B)))
