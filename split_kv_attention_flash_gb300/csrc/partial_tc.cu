@@ -27,6 +27,13 @@
 //     max grows by more than 2^8 the row's O accumulator in TMEM is rescaled first
 //     (TMEM columns 256.. / 384..). Scores are kept in base 2 (scale * log2 e).
 //   * TMEM: S0/P0 cols [0,128), S1/P1 [128,256), O0 [256,256+DV), O1 [384,384+DV).
+//   * The epilogue writes each warp's 32 rows through a swizzled 4 KB slice of the (by
+//     then idle) K stages, so that every global store covers whole 128-byte row segments.
+//   * Single-block form (KVI, launches whose M blocks hold at most 128 queries: decode
+//     with one or a few queries per sequence): tile 1 would hold only padding, so both
+//     halves work on Q0's rows -- tile t takes the key tiles 2i + t into its own S / P /
+//     O -- and the two halves are merged like two splits before anything is written.
+//     One Q tile leaves room for one more V stage.
 //   * Every mbarrier wait is bounded (1 s); a timeout records an error code in the
 //     library's device error word, raises a CTA-wide abort flag, drains in-flight
 //     TMA loads and MMAs, frees TMEM and returns.
