@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -107,15 +108,24 @@ def measured_peaks() -> dict:
     return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
+def code_text(text: str) -> str:
+    """C / C++ source without its comments, whitespace collapsed: what the compiler sees,
+    so that editing a comment does not retire a measurement of unchanged code."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def sources_sha(paths: list[str]) -> str | None:
-    """sha256 prefix of the concatenated files (a kernel's source and the headers it
-    includes), or None when one is missing."""
+    """sha256 prefix of the concatenated code of the files (a kernel's source and the
+    headers it includes, comments stripped), or None when one is missing."""
     h = hashlib.sha256()
     for rel in paths:
         src = os.path.join(ROOT, rel)
         if not os.path.exists(src):
             return None
-        h.update(open(src, "rb").read())
+        h.update(code_text(open(src, encoding="utf-8").read()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 
