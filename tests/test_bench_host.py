@@ -122,3 +122,11 @@ def test_roofline_bound_follows_the_arithmetic_intensity():
                       ("decode_small", True)):
         w = wl.ALL[name]
         assert bench.hbm_bound(bench.flops_of(w), bench.kv_bytes_of(w), peaks) == hbm, name
+
+
+def test_code_hash_ignores_comments_and_whitespace():
+    a = "int f(int x) {\n    return x + 1;  // one more\n}\n/* block\n   comment */\n"
+    b = "int f(int x) { return x + 1; }\n"
+    c = "int f(int x) { return x + 2; }\n"
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(b) != bench.code_text(c)
