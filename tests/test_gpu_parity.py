@@ -185,12 +185,16 @@ def test_large_logits_match_oracle(w):
     H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
 
 
-@pytest.mark.parametrize("dtype,mask,po", [("bf16", wl.MASK_NONE, 0), ("f16", wl.MASK_PREFIX_CAUSAL, 700)])
-def test_decode_kernel_with_several_queries(dtype, mask, po):
+@pytest.mark.parametrize("dtype,mask,po,sq", [
+    ("bf16", wl.MASK_NONE, 0, (1, 2, 3, 16, 8, 5)),
+    ("f16", wl.MASK_PREFIX_CAUSAL, 700, (1, 2, 3, 16, 8, 5)),
+    ("bf16", wl.MASK_PREFIX_CAUSAL, 500, (1, 1, 1, 1, 1, 1)),
+])
+def test_decode_kernel_with_several_queries(dtype, mask, po, sq):
     """Up to 16 queries per sequence with an M block of 64 rows: the tensor-core kernel
     (256-row M blocks) does not apply, so the CUDA-core decode kernel takes every query
     count it is templated on (1, 2, 4, 8, 16)."""
-    w = _small(dtype, 128, 128, mask=mask, po=po, S=3, bn=64, sq=(1, 2, 3, 16, 8, 5),
+    w = _small(dtype, 128, 128, mask=mask, po=po, S=3, bn=64, sq=sq,
                sk=(900, 40, 0, 1000, 777, 300))
     (q, k, v), (qd, kd, vd) = _inputs(w)
     bm = 64
@@ -281,10 +285,15 @@ def test_combine_never_reads_invalid_splits(w):
     assert not torch.isnan(out2.float()).any()
 
 
-@pytest.mark.parametrize("mask,sq", [(wl.MASK_CAUSAL, 130), (wl.MASK_NONE, 300)])
-def test_dense_layout_equals_varlen(mask, sq):
+@pytest.mark.parametrize("mask,sq,S", [(wl.MASK_CAUSAL, 130, 3), (wl.MASK_NONE, 300, 3),
+                                       (wl.MASK_NONE, 1, 3), (wl.MASK_NONE, 1, 1),
+                                       (wl.MASK_PREFIX_CAUSAL, 100, 1)])
+def test_dense_layout_equals_varlen(mask, sq, S):
+    """[B, seq, H, D] tensors without cu_seqlens give the packed layout's results bit for bit
+    (two-tile and single-block forms, partials and direct output)."""
     w = wl.Workload("dense", H=3, seqlens_q=(sq, sq), seqlens_k=(400, 400), d_qk=128, d_v=128,
-                    dtype="bf16", seed=9, n_per_block=64, split_kv=3, mask=mask)
+                    dtype="bf16", seed=9, n_per_block=64, split_kv=S, mask=mask,
+                    prefix_offset=300 if mask == wl.MASK_PREFIX_CAUSAL else 0)
     (_, _, _), (qd, kd, vd) = _inputs(w)
     out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
     p = skv.params_for(w, DEV)
