@@ -200,9 +200,11 @@ __device__ __forceinline__ void merge_block(const Problem &p, const SeqInfo &si,
 }
 
 // LPT: the (sequence, split) units -- the slowest launch dimension -- are taken longest
-// first (lpt_unit). Only instantiated for single-M-block launches (decode-like shapes with
-// a few queries per sequence), where ragged sequence lengths would otherwise leave the
-// longest sequences for the last wave; prefill launches keep the unit from blockIdx.
+// first (lpt_unit). Only instantiated for single-M-block launches of at most kLptMaxUnits
+// units (decode-like shapes with a few queries per sequence), where ragged sequence lengths
+// would otherwise leave the longest sequences for the last wave; prefill launches, and
+// single-block launches with more units, keep the unit from blockIdx.
+// KVI: the single-block form (see Cfg); DIRECT: split 1, the output written directly.
 template <typename T, int DQK, int DV, bool DIRECT, bool LPT = false, bool KVI = false>
 __global__ void __launch_bounds__(kThreads, 1)
     partial_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
