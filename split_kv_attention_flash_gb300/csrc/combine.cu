@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     constexpr int kLanes = DV / 4;
     __shared__ float sW[kMaxSplits][kRowsPerCta];
     __shared__ float sInv[kRowsPerCta];
+    ptx::wait_prior_grid();  // launched early (programmatic serialization): partials complete
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.y;
@@ -144,6 +145,25 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
 }
 
+// Launch with programmatic stream serialization: the combine's CTAs may be scheduled while
+// the partial kernel before it in the stream is finishing (it issues launch_dependents at
+// its start), and every combine kernel waits in wait_prior_grid before reading a partial.
+template <typename... Params, typename... Args>
+static cudaError_t launch_after_prior(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 namespace {
 constexpr int kBulkThreads = 128;
 constexpr int kBulkRowsDefault = 16;  // rows per CTA (measured: 32 and 8 were slower)
@@ -164,6 +184,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     __shared__ float sInv[kBulkRows];
     __shared__ int sCnt[kBulkRows];
     __shared__ volatile int sAbort;
+    ptx::wait_prior_grid();  // launched early (programmatic serialization): partials complete
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.y;
@@ -267,9 +288,8 @@ static cudaError_t launch_bulk(const Problem &p, const float *o_part, const floa
     const long long nx = (long long)row_blocks * p.B;
     if (nx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = p.S * kBulkRows * DV * 4;
-    kern<<<dim3((unsigned)nx, (unsigned)p.H), kBulkThreads, smem, st>>>(p, o_part, lse_part, counts,
-                                                                       out, lse_out, row_blocks);
-    return cudaGetLastError();
+    return launch_after_prior(kern, dim3((unsigned)nx, (unsigned)p.H), dim3(kBulkThreads), (size_t)smem, st,
+                              p, o_part, lse_part, counts, out, lse_out, row_blocks);
 }
 
 template <typename TO>
@@ -286,14 +306,12 @@ static cudaError_t launch_dv(const Problem &p, const float *o_part, const float 
     if (nx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     dim3 grid((unsigned)nx, (unsigned)p.H);
     if (p.d_v == 128)
-        combine_kernel<TO, 128><<<grid, kWarps * 32, 0, st>>>(p, o_part, lse_part, counts, out,
-                                                              lse_out, row_blocks);
-    else if (p.d_v == 64)
-        combine_kernel<TO, 64><<<grid, kWarps * 32, 0, st>>>(p, o_part, lse_part, counts, out,
-                                                             lse_out, row_blocks);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+        return launch_after_prior(combine_kernel<TO, 128>, grid, dim3(kWarps * 32), 0, st, p, o_part,
+                                  lse_part, counts, out, lse_out, row_blocks);
+    if (p.d_v == 64)
+        return launch_after_prior(combine_kernel<TO, 64>, grid, dim3(kWarps * 32), 0, st, p, o_part,
+                                  lse_part, counts, out, lse_out, row_blocks);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_combine(const Problem &p, int dtype, const float *o_part,

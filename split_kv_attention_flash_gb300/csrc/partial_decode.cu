@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kThreads, NR <= 4 ? 2 : 1)
                           float *lse_out) {
     using C = Cfg<DQK, DV>;
     extern __shared__ uint8_t smem_raw[];
+    ptx::launch_dependents();  // the combine may be scheduled onto SMs this grid leaves idle
     // CTA i of the launch order (x fastest) takes head i % H of the unit of rank i / H
     // in longest-first order (the ring's memory serves as scratch before any load)
     int h = blockIdx.y, unit = blockIdx.x;

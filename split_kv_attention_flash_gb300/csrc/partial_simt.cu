@@ -17,6 +17,7 @@
 #include <float.h>
 
 #include "sk_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace sk {
 
@@ -36,6 +37,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ float sV[kKT][DV];
     __shared__ float sP[kRows][kKT + 1];
     __shared__ int sRange[2];
+    ptx::launch_dependents();  // the combine may be scheduled onto SMs this grid leaves idle
 
     const int tid = threadIdx.x;
     const int r = tid / kTpr, c = tid % kTpr;

@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<DQK, DV, KVI>;
     constexpr bool kBF16 = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value;
     extern __shared__ uint8_t smem_raw[];
+    ptx::launch_dependents();  // the combine may be scheduled onto SMs this grid leaves idle
 
     const int mb = blockIdx.x, h = blockIdx.y;
     int s, b;

@@ -15,6 +15,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// Programmatic dependent launch. launch_dependents: the kernel launched after this one in
+// the stream (with programmatic stream serialization) may start once every CTA of this grid
+// has issued it or exited. wait_prior_grid: returns once the grid this one follows has
+// completed and its memory operations are visible (at once when there is none).
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
