@@ -275,7 +275,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     def step():
         skv.sk_attn_fwd(p, q, k, v, out, lse, ws)
 
-    fused = bool(p.fuse_combine) and kname in ("partial_tc", "partial_tc2") and S <= 8
+    fused = bool(p.fuse_combine) and kname == "partial_tc" and S <= 8
     launches_per_step = 1 if S == 1 or fused else 2   # partial, combine
     sampler = ClockSampler(dev.index)
     with sampler:

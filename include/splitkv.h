@@ -183,9 +183,13 @@ sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
  *   - Problems whose sk_workspace_bytes() exceeds SK_STATIC_SCRATCH_BYTES are
  *     rejected with SK_ERR_WORKSPACE before anything is launched.
  *   - It calls no cudaMalloc / cudaFree and no allocating library routine.
- *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current); make that first call before any stream
- *     capture.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and keeps it; make that first call before any stream capture.
+ *     A lookup that fails is not kept: the call returns SK_ERR_CUDA (the error is in
+ *     sk_last_cuda_error) and the next call tries again.
+ *   - The kept address belongs to the device's current context: do not call this
+ *     entry point again after cudaDeviceReset (or anything else that destroys and
+ *     recreates the context) in the same process.
  *   - Every call on a device shares the one array and leaves its contents behind;
  *     nothing in it has to start at zero (each call writes what it later reads).
  *     Calls that overlap on the GPU (other streams, other threads) race on it.
@@ -220,7 +224,8 @@ int sk_default_block_m(int d_qk, int d_v, sk_dtype dtype);
 int sk_supported_head_dims(int d_qk, int d_v);
 
 /* Name of the kernel sk_attn_partial_fwd would launch for these parameters, for
- * logging and benchmarks; NULL when the call would be rejected. */
+ * logging and benchmarks; NULL when the call would be rejected. split_kv = 0 is
+ * resolved as sk_auto_split_kv resolves it (reading the current device). */
 const char *sk_partial_kernel_name(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v);
 
 /* Human-readable text of a status code. */

@@ -16,16 +16,24 @@ __device__ int g_device_error;
 
 constexpr int kMaxDevices = 64;
 int *g_err_ptr[kMaxDevices];
-std::once_flag g_err_once[kMaxDevices];
+std::mutex g_err_mutex;
 
+// Device address of the error word on the current device. Only a successful lookup is
+// kept, so a lookup that failed (a sticky error pending, a call made during stream
+// capture) is tried again by the next call.
 int *device_error_word() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::call_once(g_err_once[dev], [dev] {
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if (!g_err_ptr[dev]) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_device_error) == cudaSuccess) g_err_ptr[dev] = (int *)ptr;
         else (void)cudaGetLastError();
-    });
+    }
     return g_err_ptr[dev];
 }
 
@@ -128,6 +136,14 @@ sk_status cuda_status(cudaError_t e) {
     t_last_cuda_error = (int)e;
     return SK_ERR_CUDA;
 }
+
+}  // namespace
+
+namespace sk {
+sk_status record_cuda_error(cudaError_t e) { return cuda_status(e); }
+}  // namespace sk
+
+namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -254,7 +270,8 @@ sk_status sk_valid_split_counts(const sk_params *p, int32_t *counts, sk_stream s
 
 const char *sk_partial_kernel_name(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v) {
     if (check_params(p) != SK_OK || check_qkv(p, q, k, v) != SK_OK) return nullptr;
-    int S = p->split_kv > 0 ? p->split_kv : 1;
+    int S = 0;
+    if (resolve_split(p, &S) != SK_OK) return nullptr;  // split_kv = 0: the automatic choice
     return sk::partial_kernel_name(make_problem(p, S), q.dtype, view(q), view(k), view(v));
 }
 

@@ -135,10 +135,6 @@ __host__ __device__ inline void split_key_range(const Problem &p, int sq, int la
     ke = (int)(e < bl + 1 ? e : bl + 1);
 }
 
-// Splits that the partition of the M block holding query `pos` leaves non-empty: the
-// first ceil(tiles / itersPerBlock) of them. The merge never reads the others ([P1]
-// review notes on a real early exit: a split with nothing to do may write nothing,
-// so the merge must not assume its memory was written).
 // Longest-first launch order. The CTAs of a (sequence, split) unit all stream that
 // split's keys; with sequences of very different lengths, launching the units in
 // index order can leave the longest ones for the last wave. lpt_unit returns the unit
@@ -172,6 +168,10 @@ __device__ inline int lpt_unit(const Problem &p, int r, int n, int *keys, int *f
     return u;
 }
 
+// Splits that the partition of the M block holding query `pos` leaves non-empty: the
+// first ceil(tiles / itersPerBlock) of them. The merge never reads the others ([P1]
+// review notes on a real early exit: a split with nothing to do may write nothing,
+// so the merge must not assume its memory was written).
 __host__ __device__ inline int nonempty_splits(const Problem &p, int sq, int last_valid, int pos) {
     long long first = (long long)(pos / p.bm) * p.bm;
     long long last_row = first + p.bm - 1;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include "sk_common.cuh"
+#include "splitkv.h"
 
 namespace sk {
 
@@ -20,6 +21,10 @@ cudaError_t run_partial_fused(const Problem &p, int dtype, const TensorView &q,
                               const TensorView &k, const TensorView &v, float *o_part,
                               float *lse_part, const TensorView &out, float *lse_out, int *tickets,
                               cudaStream_t st, bool *fused);
+
+// Records `e` as the calling thread's last CUDA error (sk_last_cuda_error) and returns
+// SK_ERR_CUDA, or SK_OK for cudaSuccess.
+sk_status record_cuda_error(cudaError_t e);
 
 // Name of the kernel run_partial would launch.
 const char *partial_kernel_name(const Problem &p, int dtype, const TensorView &q,

@@ -502,3 +502,104 @@ def test_combine_never_reads_partition_empty_splits(w):
     skv.sk_combine(p, o_bad, l_bad, counts, out2, lse2)
     torch.cuda.synchronize()
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+# ------------------------------------------- every public path against the oracle
+#
+# "Recombine fully masked split-KV attention partials on the host", Technical details:
+# the NaN-safe f32 merge over the splits s < count. Besides sk_attn_fwd (above), the
+# library exposes two more ways of getting the merged output; each is compared here with
+# the f64 oracle, element by element, at the stated tolerances.
+
+def _three_call(w, qd, kd, vd, S, with_lse=True):
+    """sk_attn_partial_fwd -> sk_valid_split_counts -> sk_combine with the caller's counts."""
+    o_part, l_part, p = H.run_partials(w, qd, kd, vd, DEV, S)
+    counts = torch.full((w.total_q,), -7, dtype=torch.int32, device=DEV)
+    skv.sk_valid_split_counts(p, counts)
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=qd.dtype, device=DEV)
+    lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=DEV) if with_lse else None
+    skv.sk_combine(p, o_part, l_part, counts, out, lse)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+@pytest.mark.parametrize("w", SMALL + LIMITS, ids=lambda w: w.name)
+def test_three_call_path_matches_oracle(w):
+    """The standalone public path, with the counts array the caller got from
+    sk_valid_split_counts, against unsplit attention; without an LSE output the output is
+    identical."""
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    S = H.resolved_split(w, DEV)
+    out, lse = _three_call(w, qd, kd, vd, S)
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, f"three calls S={S}")
+    out2, _ = _three_call(w, qd, kd, vd, S, with_lse=False)
+    assert torch.equal(out, out2)
+
+
+def _oracle_partials_on_device(prob, q, k, v):
+    """The oracle's partials, rounded to f32 (the workspace's type), in the library's
+    [H, S, total_q, d_v] / [H, S, total_q] layout, plus the f32 values as f64 arrays."""
+    po, pl = oracle.partials(prob, q, k, v)                    # [n, H, S, dv], [n, H, S]
+    po32, pl32 = po.astype(np.float32), pl.astype(np.float32)
+    o_dev = torch.from_numpy(np.ascontiguousarray(po32.transpose(1, 2, 0, 3))).to(DEV)
+    l_dev = torch.from_numpy(np.ascontiguousarray(pl32.transpose(1, 2, 0))).to(DEV)
+    return o_dev, l_dev, po32.astype(np.float64), pl32.astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 8, 9, 16, 32])
+def test_combine_of_oracle_partials_matches_oracle_merge(S, dtype):
+    """sk_combine alone, fed the oracle's own partials and counts: its output and LSE against
+    the oracle's merge of the same f32 values. Covers the bulk-copy form (S <= 8), the
+    register-prefetch form (S > 8), fully masked rows (prefix offset < 0, a sequence without
+    keys), rows whose count is below S, and splits s >= count filled with NaN, which the
+    merge must never read."""
+    w = _small(dtype, 128, 128, mask=wl.MASK_PREFIX_CAUSAL, po=-50, S=S, bn=16,
+               sq=(300, 40, 0, 7), sk=(900, 600, 30, 0), seed=S)
+    q, k, v = w.make_inputs("cpu")
+    prob = H.oracle_problem(w, S)
+    counts = oracle.split_counts(prob)
+    o_dev, l_dev, po, pl = _oracle_partials_on_device(prob, q, k, v)
+    invalid = torch.arange(S, device=DEV)[None, :, None] >= torch.from_numpy(counts).to(DEV)[None, None, :]
+    o_dev = o_dev.masked_fill(invalid[..., None], float("nan"))
+    l_dev = l_dev.masked_fill(invalid, float("nan"))
+    p = skv.params_for(w, DEV, split_kv=S)
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=w.torch_dtype, device=DEV)
+    lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=DEV)
+    skv.sk_combine(p, o_dev, l_dev, torch.from_numpy(counts).to(DEV), out, lse)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.merge(po, pl, counts)
+    assert np.isneginf(ref_l).any() and (counts < S).any() or S == 1
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, dtype, f"combine S={S}")
+    # the merge itself runs in f32: before the cast to the storage type it is within f32
+    # rounding of the oracle's f64 merge of the same values
+    if dtype == "f32":
+        assert np.abs(H.to_np(out) - ref_o).max() <= 4e-6
+
+
+FUSED = [w for w in SMALL + LIMITS if w.dtype != "f32" and 2 <= w.split_kv <= 8]
+
+
+@pytest.mark.parametrize("w", FUSED, ids=lambda w: w.name)
+def test_fused_merge_matches_oracle(w):
+    """sk_attn_fwd with fuse_combine = 1: the tensor-core kernel's last CTA of each M block
+    merges the splits. Compared with unsplit attention; a second call over the same workspace
+    (tickets cleared again) gives identical results, and so does a call without LSE."""
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    out, lse, p = H.run_fwd(w, qd, kd, vd, DEV, fuse_combine=1)
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "fused merge")
+    out2, lse2, _ = H.run_fwd(w, qd, kd, vd, DEV, fuse_combine=1)
+    out3, _, _ = H.run_fwd(w, qd, kd, vd, DEV, fuse_combine=1, with_lse=False)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2) and torch.equal(out, out3)
+
+
+def test_fused_merge_matches_oracle_full_size():
+    """The fused merge on the target shape (automatic split, 3), sampled rows."""
+    w = wl.TARGET_SHAPE
+    q, k, v = w.make_inputs(DEV)
+    rows = H.sample_rows(w, head=32, tail=32, rand=64)
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q.cpu(), k.cpu(), v.cpu(), rows=rows)
+    out, lse, _ = H.run_fwd(w, q, k, v, DEV, fuse_combine=1)
+    H.assert_close(H.to_np(out, rows), H.lse_np(lse, rows), ref_o, ref_l, w.dtype, "fused target")

@@ -41,12 +41,21 @@ CASES = [
                 prefix_offset=5000),
     wl.Workload("f32 causal", H=2, seqlens_q=(64, 90), seqlens_k=(256, 300), d_qk=64, d_v=64,
                 dtype="f32", seed=23, n_per_block=32, split_kv=4, mask=wl.MASK_CAUSAL),
+    # the merge fused into the tensor-core kernel (256-row M blocks): its tickets live in
+    # the shared scratch too, are cleared by every call and counted up again
+    wl.Workload("fused merge", H=3, seqlens_q=(600, 257, 40), seqlens_k=(5000, 1300, 900),
+                d_qk=128, d_v=128, dtype="bf16", seed=24, n_per_block=128, split_kv=4,
+                mask=wl.MASK_PREFIX_CAUSAL, prefix_offset=700, extra={"fuse_combine": 1}),
 ]
+
+
+def _params(w):
+    return skv.params_for(w, DEV, fuse_combine=w.extra.get("fuse_combine", 0))
 
 
 def _run(w, seed, static):
     q, k, v = w.with_(seed=seed).make_inputs(DEV)
-    p = skv.params_for(w, DEV)
+    p = _params(w)
     out = torch.empty(w.total_q, w.H, w.d_v, dtype=q.dtype, device=DEV)
     lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=DEV)
     if static:
@@ -60,7 +69,7 @@ def _run(w, seed, static):
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_static_entry_matches_workspace_entry_on_two_calls(w):
-    assert skv.sk_workspace_bytes(skv.params_for(w, DEV)) <= skv.SK_STATIC_SCRATCH_BYTES
+    assert skv.sk_workspace_bytes(_params(w)) <= skv.SK_STATIC_SCRATCH_BYTES
     for seed in (w.seed, w.seed + 100):          # two calls in a row, different inputs
         ref_o, ref_l = _run(w, seed, static=False)
         got_o, got_l = _run(w, seed, static=True)
@@ -82,3 +91,21 @@ def test_static_entry_rejects_problems_above_its_scratch():
     with pytest.raises(skv.SplitKVError) as ei:
         skv.sk_attn_fwd_static(p, q, k, v, out)
     assert ei.value.status == 3  # SK_ERR_WORKSPACE
+
+
+def test_static_entry_allocates_no_device_memory():
+    """After a first call (which looks up the scratch array and loads the kernels), a call
+    leaves both torch's allocator and the device's free memory unchanged."""
+    w = CASES[1]
+    q, k, v = w.make_inputs(DEV)
+    p = _params(w)
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=q.dtype, device=DEV)
+    lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=DEV)
+    skv.sk_attn_fwd_static(p, q, k, v, out, lse)
+    torch.cuda.synchronize()
+    allocated = torch.cuda.memory_allocated(DEV)
+    free_before = torch.cuda.mem_get_info(DEV)[0]
+    skv.sk_attn_fwd_static(p, q, k, v, out, lse)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info(DEV)[0] == free_before
+    assert torch.cuda.memory_allocated(DEV) == allocated
