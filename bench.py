@@ -171,15 +171,28 @@ def kv_bytes_of(w) -> float:
 
 
 class ClockSampler:
+    """nvidia-smi samples (every 50 ms) of one GPU while the `with` block runs. Entering
+    waits (up to 5 s) for the first sample, so that a loop of about a second is sampled
+    from its start."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, keep_first: bool = False, trailing: bool = False):
         self.idx = device_index
         self.proc = None
+        self.lines = []
+        self.keep_first = keep_first  # keep the samples taken before the work started
+        self.trailing = trailing      # wait for one sample after the work (short loops)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.lines.append(line)
 
     def __enter__(self):
+        import threading
+        self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
@@ -187,18 +200,29 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.first = 0 if self.keep_first else len(self.lines)
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
+            if self.trailing:
+                n, t0 = len(self.lines), time.time()
+                while len(self.lines) == n and time.time() - t0 < 1.0 and self.proc.poll() is None:
+                    time.sleep(0.005)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self.proc.wait()
+            self.reader.join(timeout=5)
+            self.lines = self.lines[self.first:]
 
     def summary(self):
         rows = []
@@ -209,7 +233,7 @@ class ClockSampler:
             except (ValueError, IndexError):
                 continue
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         loaded = [r for r in rows if r[2] >= 50] or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v == "Active"})
@@ -248,6 +272,121 @@ def time_oracle(w, target_s: float, seed: int = 0, inputs=None):
 
 # ------------------------------------------------------------------- our arm
 
+def timed_chunks(run_chunk, per_chunk: int, min_s: float, stream) -> dict:
+    """Back-to-back chunks of `per_chunk` launches for at least `min_s` seconds of device
+    time, each chunk bracketed by CUDA events on `stream`; the host enqueues every chunk
+    before it waits. mean_ms = total time / launches (the average launch duration);
+    median_ms = median over chunks of the chunk's time per launch."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    run_chunk()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    n = max(10, int(min_s / max(e0.elapsed_time(e1) * 1e-3, 1e-6)) + 1)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for i in range(n):
+        run_chunk()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    return {"mean_ms": sum(ms) / (n * per_chunk), "median_ms": statistics.median(ms) / per_chunk,
+            "launches": n * per_chunk, "seconds": sum(ms) * 1e-3}
+
+
+def time_back_to_back(launch, min_s: float, stream, rotate: int = 1) -> dict:
+    """Device time per launch of `launch(i)` (i picks one of `rotate` buffer sets) run back
+    to back for at least `min_s` seconds. Launches shorter than 0.2 ms are captured into a
+    CUDA graph of a few milliseconds of launches and replayed, so that the host's call
+    overhead (a ctypes call takes some 10-20 us) cannot leave gaps between them."""
+    for i in range(3):
+        launch(i % rotate)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    launch(0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    one_ms = e0.elapsed_time(e1)
+    if one_ms < 0.2:
+        per = max(rotate, int(2.0 / max(one_ms, 1e-3)))
+        per = rotate * -(-per // rotate)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(per):
+                launch(i % rotate)
+        graph.replay()
+        r = timed_chunks(graph.replay, per, min_s, stream)
+        r["graph_launches"] = per
+        del graph
+        return r
+    state = {"i": 0}
+
+    def one():
+        launch(state["i"] % rotate)
+        state["i"] += 1
+    return timed_chunks(one, 1, min_s, stream)
+
+
+def roofline_of(w, kname: str, fl: float, loop: dict, peaks: dict, traffic, clocks) -> dict:
+    """The partial kernel's roofline entry: tensor-bound (TFLOP/s against the measured dense
+    bf16 peak, burst and sustained) for prefill shapes, HBM-bound (K and V bytes per second
+    against the measured copy bandwidth) for decode shapes."""
+    ms = loop["mean_ms"]
+    common = {"kernel": kname, "ms_per_launch": ms, "ms_per_launch_median": loop["median_ms"],
+              "launches": loop["launches"], "seconds": loop["seconds"], "traffic": traffic,
+              "clocks": clocks}
+    if hbm_bound(fl, kv_bytes_of(w), peaks):   # a stream over K and V: bound by HBM
+        gbs = kv_bytes_of(w) / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm"], "peak_source": f"{peaks['source']} HBM copy",
+                "bytes_per_launch": kv_bytes_of(w), **common}
+    tf = fl / (ms * 1e-3) / 1e12
+    out = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s",
+           "frac": tf / peaks["bf16"], "peak_source": f"{peaks['source']} dense bf16 burst",
+           "flop_per_launch": fl, **common}
+    if peaks.get("bf16_sustained"):
+        out["peak_sustained"] = peaks["bf16_sustained"]
+        out["frac_sustained"] = tf / peaks["bf16_sustained"]
+    return out
+
+
+def kernel_blocks(skv, w, p, q, k, v, S: int, kname: str, peaks: dict, min_s: float, dev, stream):
+    """The partial kernel alone and the combine alone, each timed back to back for at least
+    `min_s` seconds with the clocks sampled during its loop. The combine runs over rotating
+    copies of the partials that together exceed L2 three times, so that every launch reads
+    its inputs from HBM."""
+    fl = flops_of(w)
+    o_part = torch.empty(w.H, S, w.total_q, w.d_v, dtype=torch.float32, device=dev)
+    l_part = torch.empty(w.H, S, w.total_q, dtype=torch.float32, device=dev)
+    with ClockSampler(dev.index) as cs:
+        loop = time_back_to_back(lambda i: skv.sk_attn_partial_fwd(p, q, k, v, o_part, l_part),
+                                 min_s, stream)
+    roof = roofline_of(w, kname, fl, loop, peaks, None, cs.summary())
+    comb = None
+    counts = torch.empty(w.total_q, dtype=torch.int32, device=dev)
+    skv.sk_valid_split_counts(p, counts)
+    if S > 1:
+        out = torch.empty(w.total_q, w.H, w.d_v, dtype=q.dtype, device=dev)
+        part_bytes = (o_part.numel() + l_part.numel()) * 4
+        n_copies = max(2, -(-3 * L2_BYTES // max(part_bytes, 1)))
+        copies = [(o_part, l_part)] + [(o_part.clone(), l_part.clone()) for _ in range(n_copies - 1)]
+        with ClockSampler(dev.index) as cs:
+            cl = time_back_to_back(lambda i: skv.sk_combine(p, *copies[i], counts, out, None),
+                                   min_s, stream, rotate=n_copies)
+        cbytes = combine_bytes(w, counts.cpu().numpy(), with_lse=False)
+        gbs = cbytes / (cl["mean_ms"] * 1e-3) / 1e9
+        comb = {"achieved": gbs, "unit": "GB/s", "peak": peaks["hbm"], "frac": gbs / peaks["hbm"],
+                "bytes": cbytes, "us_per_launch": cl["mean_ms"] * 1e3,
+                "us_per_launch_median": cl["median_ms"] * 1e3, "launches": cl["launches"],
+                "seconds": cl["seconds"], "clocks": cs.summary(),
+                "l2": f"back-to-back launches (CUDA graph of {cl.get('graph_launches', 1)}) over "
+                      f"{n_copies} rotating partial copies >= 3x L2"}
+        del copies
+    return roof, comb, counts
+
+
 def run_ours(args, rank: int, world: int, dist_on: bool):
     import split_kv_attention_flash_gb300 as skv
     from split_kv_attention_flash_gb300 import _build
@@ -271,13 +410,16 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     kname = skv.sk_partial_kernel_name(p, q, k, v)
     fl = flops_of(w)
     stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
 
     def step():
         skv.sk_attn_fwd(p, q, k, v, out, lse, ws)
 
-    fused = bool(p.fuse_combine) and kname == "partial_tc" and S <= 8
+    fused = bool(p.fuse_combine) and kname.startswith("partial_tc") and S <= 8
     launches_per_step = 1 if S == 1 or fused else 2   # partial, combine
-    sampler = ClockSampler(dev.index)
+    # the timed steps may last only milliseconds: keep every sample from the warm-up on and
+    # one taken right after the last step
+    sampler = ClockSampler(dev.index, keep_first=True, trailing=True)
     with sampler:
         for _ in range(args.warmup):
             step()
@@ -294,117 +436,87 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         if dist_on:
             torch.distributed.barrier()
         ms = e0.elapsed_time(e1) / args.steps
-
-        # the partial kernel alone (dominant kernel), same stream
-        o_part = torch.empty(w.H, S, w.total_q, w.d_v, dtype=torch.float32, device=dev)
-        l_part = torch.empty(w.H, S, w.total_q, dtype=torch.float32, device=dev)
-        for _ in range(3):
-            skv.sk_attn_partial_fwd(p, q, k, v, o_part, l_part)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        n_part = max(args.steps, 5)
-        for _ in range(n_part):
-            skv.sk_attn_partial_fwd(p, q, k, v, o_part, l_part)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        part_ms = e0.elapsed_time(e1) / n_part
-
-        # the combine alone: back to back over rotating copies of the partials that
-        # together exceed L2 three times, so every launch reads its inputs from HBM
-        counts = torch.empty(w.total_q, dtype=torch.int32, device=dev)
-        skv.sk_valid_split_counts(p, counts)
-        part_bytes = (o_part.numel() + l_part.numel()) * 4
-        n_copies = max(2, -(-3 * L2_BYTES // max(part_bytes, 1)))
-        copies = [(o_part, l_part)] + [(o_part.clone(), l_part.clone()) for _ in range(n_copies - 1)]
-        for i in range(3):
-            skv.sk_combine(p, *copies[i % n_copies], counts, out, None)
-        torch.cuda.synchronize()
-        n_comb = max(args.steps, 10 * n_copies)
-        e0.record(stream)
-        for i in range(n_comb):
-            skv.sk_combine(p, *copies[i % n_copies], counts, out, None)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        comb_ms = e0.elapsed_time(e1) / n_comb
-        del copies
-
-        # end to end through the public call: every step copies its Q, K, V in from pinned
-        # host memory and its output back out. Two device buffer sets let step i + 1's
-        # inputs and step i's output travel on their own streams while steps compute in
-        # order on the compute stream (the copies stay inside the timed region).
-        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-        bufs = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out))
-                for _ in range(2)]
-        h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        copied = [torch.cuda.Event() for _ in range(2)]
-        computed = [torch.cuda.Event() for _ in range(2)]
-        drained = [torch.cuda.Event() for _ in range(2)]
-
-        def e2e_run(n_steps):
-            start = torch.cuda.Event()
-            start.record(stream)
-            h2d.wait_event(start)
-
-            def issue_h2d(i):
-                b = i % 2
-                if i >= 2:
-                    h2d.wait_event(computed[b])   # step i - 2 is done with this set's inputs
-                with torch.cuda.stream(h2d):
-                    for dst, src in zip(bufs[b][:3], (hq, hk, hv)):
-                        dst.copy_(src, non_blocking=True)
-                    copied[b].record(h2d)
-
-            issue_h2d(0)
-            for i in range(n_steps):
-                b = i % 2
-                if i + 1 < n_steps:
-                    issue_h2d(i + 1)
-                stream.wait_event(copied[b])
-                if i >= 2:
-                    stream.wait_event(drained[b])  # step i - 2's output has been read back
-                skv.sk_attn_fwd(p, bufs[b][0], bufs[b][1], bufs[b][2], bufs[b][3], None, ws)
-                computed[b].record(stream)
-                d2h.wait_event(computed[b])
-                with torch.cuda.stream(d2h):
-                    hout[b].copy_(bufs[b][3], non_blocking=True)
-                    drained[b].record(d2h)
-            stream.wait_stream(d2h)
-
-        e2e_run(3)
-        torch.cuda.synchronize()
-        n_e2e = max(args.steps // 4, 5)
-        e0.record(stream)
-        e2e_run(n_e2e)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
     clocks = sampler.summary()
+    if args.step_only:  # profiling runs: the timed steps and nothing else
+        ms = max_over_ranks([ms], device=dev if dist_on else None)[0]
+        if rank != 0:
+            return None
+        return {"metric": METRIC, "value": whole_job_tflops(fl, world, ms), "unit": UNIT,
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+                "config": {**shape_config(w), "split_kv": S, "step_only": True},
+                "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+
+    # the dominant kernel and the combine, each alone, seconds-long loops
+    roof, comb, counts = kernel_blocks(skv, w, p, q, k, v, S, kname, peaks, args.loop_seconds,
+                                       dev, stream)
+    roof["traffic"] = recorded_traffic(kname, args.workload)
+    if launches_per_step == 1 and not fused:
+        roof["note"] = "split 1: a step is this kernel writing the output directly"
+
+    # end to end through the public call: every step copies its Q, K, V in from pinned
+    # host memory and its output back out. Two device buffer sets let step i + 1's inputs
+    # and step i's output travel on their own streams while steps compute in order on the
+    # compute stream (the copies stay inside the timed region).
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    bufs = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out))
+            for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_run(n_steps):
+        start = torch.cuda.Event()
+        start.record(stream)
+        h2d.wait_event(start)
+
+        def issue_h2d(i):
+            b = i % 2
+            if i >= 2:
+                h2d.wait_event(computed[b])   # step i - 2 is done with this set's inputs
+            with torch.cuda.stream(h2d):
+                for dst, src in zip(bufs[b][:3], (hq, hk, hv)):
+                    dst.copy_(src, non_blocking=True)
+                copied[b].record(h2d)
+
+        issue_h2d(0)
+        for i in range(n_steps):
+            b = i % 2
+            if i + 1 < n_steps:
+                issue_h2d(i + 1)
+            stream.wait_event(copied[b])
+            if i >= 2:
+                stream.wait_event(drained[b])  # step i - 2's output has been read back
+            skv.sk_attn_fwd(p, bufs[b][0], bufs[b][1], bufs[b][2], bufs[b][3], None, ws)
+            computed[b].record(stream)
+            d2h.wait_event(computed[b])
+            with torch.cuda.stream(d2h):
+                hout[b].copy_(bufs[b][3], non_blocking=True)
+                drained[b].record(d2h)
+        stream.wait_stream(d2h)
+
+    e2e_run(3)
+    torch.cuda.synchronize()
+    n_e2e = max(args.steps // 4, 5)
+    e0.record(stream)
+    e2e_run(n_e2e)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    del hq, hk, hv, hout, bufs
 
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev if dist_on else None)
+    varlen = None
+    if world == 1 and args.workload != "varlen" and not args.no_varlen:
+        del q, k, v, ws, out
+        torch.cuda.empty_cache()
+        varlen = varlen_block(skv, args, peaks, dev, stream)
     if rank != 0:
         return None
 
-    peaks = measured_peaks()
-    counts_np = counts.cpu().numpy()
-    cbytes = combine_bytes(w, counts_np, with_lse=False)
-    if launches_per_step == 1 and not fused:
-        # S == 1: a step is exactly one launch of the partial kernel writing the output
-        # directly, so the step time is that kernel's time as the step runs it
-        part_ms = ms
-    part_tflops = fl / (part_ms * 1e-3) / 1e12
-    traffic = recorded_traffic(kname, args.workload)
-    if hbm_bound(fl, kv_bytes_of(w), peaks):   # a stream over K and V: bound by HBM
-        gbs = kv_bytes_of(w) / (part_ms * 1e-3) / 1e9
-        roofline = {"kernel": kname, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm"],
-                    "unit": "GB/s", "frac": gbs / peaks["hbm"],
-                    "peak_source": f"{peaks['source']} HBM copy", "ms_per_launch": part_ms,
-                    "bytes_per_launch": kv_bytes_of(w), "traffic": traffic}
-    else:
-        roofline = {"kernel": kname, "bound": "tensor", "achieved": part_tflops,
-                    "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": part_tflops / peaks["bf16"],
-                    "peak_source": f"{peaks['source']} dense bf16 burst",
-                    "ms_per_launch": part_ms, "flop_per_launch": fl, "traffic": traffic}
     line = {
         "metric": METRIC, "value": whole_job_tflops(fl, world, ms), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -415,25 +527,50 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
                    "split_kv": S, "fuse_combine": p.fuse_combine,
                    "block_m": skv.sk_default_block_m(w.d_qk, w.d_v),
                    "l2": "inputs larger than L2 "
-                   f"({(q.numel() + k.numel() + v.numel()) * q.element_size() / 1e6:.0f} MB)",
+                   f"({(w.total_q * w.d_qk + w.total_k * (w.d_qk + w.d_v)) * w.H * (4 if w.dtype == 'f32' else 2) / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roofline,
-        "combine": {"achieved": cbytes / (comb_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "peak": peaks["hbm"], "frac": cbytes / (comb_ms * 1e-3) / 1e9 / peaks["hbm"],
-                    "bytes": cbytes, "us_per_launch": comb_ms * 1e3,
-                    "l2": "back-to-back launches over rotating partial copies >= 3x L2"},
+        "roofline": roof,
+        "combine": comb,
         "e2e": {"value": whole_job_tflops(fl, world, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * q.element_size()),
-                "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "h2d_bytes_per_step": int(w.H * (w.total_q * w.d_qk + w.total_k * (w.d_qk + w.d_v))
+                                          * (4 if w.dtype == "f32" else 2)),
+                "d2h_bytes_per_step": int(w.total_q * w.H * w.d_v * (4 if w.dtype == "f32" else 2)),
                 "ms_per_step": e2e_ms,
                 "overlap": "step i+1's host-to-device copies and step i's read-back run on their "
                            "own streams beside step i's compute"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if varlen is not None:
+        line["varlen"] = varlen
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(w, args.cpu_seconds)
     return line
+
+
+def varlen_block(skv, args, peaks: dict, dev, stream) -> dict:
+    """The long-context packed varlen prefill (4 x Sq 4096, Sk 8192 / 42700 / 65536 / 131072,
+    H 12, D 192/128, split automatic): the whole step, the partial kernel alone against the
+    dense bf16 peak and the combine alone against HBM, in the same run as the main line."""
+    w = wl.LONG_VARLEN
+    q, k, v = w.make_inputs(dev)
+    p = skv.params_for(w, dev)
+    S = skv.sk_auto_split_kv(p)
+    p.split_kv = S
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=q.dtype, device=dev)
+    ws = torch.empty(max(skv.sk_workspace_bytes(p), 1), dtype=torch.uint8, device=dev)
+    kname = skv.sk_partial_kernel_name(p, q, k, v)
+    fl = flops_of(w)
+    with ClockSampler(dev.index) as cs:
+        st = time_back_to_back(lambda i: skv.sk_attn_fwd(p, q, k, v, out, None, ws),
+                               args.loop_seconds, stream)
+    roof, comb, _ = kernel_blocks(skv, w, p, q, k, v, S, kname, peaks, args.loop_seconds, dev,
+                                  stream)
+    roof["traffic"] = recorded_traffic(kname, "varlen")
+    return {"workload": w.name, "split_kv": S, "flop_per_step": fl,
+            "ms_per_step": st["mean_ms"], "step_tflops": fl / (st["mean_ms"] * 1e-3) / 1e12,
+            "steps": st["launches"], "step_clocks": cs.summary(), "partial": roof,
+            "combine": comb}
 
 
 def shape_config(w) -> dict:
@@ -483,6 +620,13 @@ def main():
                     help="merge the splits inside the tensor-core kernel (sk_params.fuse_combine)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--loop-seconds", type=float, default=1.0,
+                    help="device time of each kernel-alone loop (partial kernel, combine)")
+    ap.add_argument("--no-varlen", action="store_true",
+                    help="skip the long-context varlen block of the JSON line")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time the steps only (no kernel loops, end-to-end, varlen block or CPU "
+                         "baseline): the command the profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -9,12 +9,12 @@
 // The pass is HBM-bound: it reads count * (4 d_v + 4) bytes and writes d_v
 // storage-type elements (+ 4 bytes of LSE) per (head, row).
 //
-// combine_bulk_kernel (S <= 8): a CTA merges 16 consecutive rows of one head. For a
-// (head, split) plane those rows are one contiguous chunk of 16 * d_v floats, so one
-// thread first issues one bulk asynchronous copy per split into shared memory (the
-// splits the partition leaves non-empty for the M block), then warp 0 forms the
-// counts and weights while they land; then every warp merges 4 rows out of shared
-// memory.
+// combine_bulk_kernel (S <= 8): a CTA merges 16 consecutive packed rows of one head,
+// whichever sequences they belong to. For a (head, split) plane those rows are one
+// contiguous chunk of 16 * d_v floats, so one thread first issues one bulk asynchronous
+// copy per split into shared memory, before any load the copies would depend on; warp 0
+// finds each row's sequence, count and weights while they land; then every warp merges
+// 4 rows out of shared memory.
 //
 // combine_kernel (any S <= 32): a CTA merges 32 consecutive rows of one head:
 //   * every warp reads the counts of its 4 rows and at once issues the 16-byte
@@ -166,68 +166,101 @@ static cudaError_t launch_after_prior(void (*kern)(Params...), dim3 grid, dim3 b
 
 namespace {
 constexpr int kBulkThreads = 128;
-constexpr int kBulkRowsDefault = 16;  // rows per CTA (measured: 32 and 8 were slower)
+constexpr int kBulkRows = 16;  // packed rows per CTA (measured: 8 rows / 64 threads and
+                               // 32 rows / 256 threads no faster, 32 rows / 128 threads slower)
 constexpr int kBulkMaxSplits = 8;
 constexpr uint64_t kBulkTimeoutNs = 1000000000ull;
 }  // namespace
 
-template <typename TO, int DV, int kBulkRows>
+// Sequence holding packed query row `row`: the last b with cu_q[b] <= row (binary search;
+// bad cu_seqlens give a wrong b in [0, B), never an index outside cu_q), or row / max_sq in
+// the dense layout. Sets *pos to the row's position in that sequence.
+__device__ inline int seq_of_row(const Problem &p, int row, int *pos) {
+    if (!p.cu_q) {
+        const int b = row / p.max_sq;
+        *pos = row - b * p.max_sq;
+        return b;
+    }
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.cu_q + mid) <= row) lo = mid;
+        else hi = mid - 1;
+    }
+    *pos = row - __ldg(p.cu_q + lo);
+    return lo;
+}
+
+// A CTA merges 16 consecutive packed rows of one head, whichever sequences they belong
+// to. The rows of a (head, split) plane are contiguous, so the first thread issues the S
+// bulk copies before anything else is known; meanwhile warp 0 (one lane per row) loads
+// the row's S log-sum-exps, finds its sequence, count and weights. Splits that the
+// partition leaves empty are copied but never read (their memory may be unwritten).
+template <typename TO, int DV>
 __global__ void __launch_bounds__(kBulkThreads)
     combine_bulk_kernel(Problem p, const float *__restrict__ o_part,
                         const float *__restrict__ lse_part, const int32_t *__restrict__ counts,
-                        TensorView out, float *__restrict__ lse_out, int row_blocks) {
+                        TensorView out, float *__restrict__ lse_out) {
     static_assert(DV % 4 == 0 && DV / 4 <= 32, "one float4 per lane");
     constexpr int kLanes = DV / 4;
+    constexpr int kRowsPerWarp = kBulkRows / (kBulkThreads / 32);
     extern __shared__ __align__(128) uint8_t sO_raw[];   // [split][kBulkRows rows][DV] f32
     __shared__ __align__(8) uint64_t sBar;
     __shared__ float sW[kBulkMaxSplits][kBulkRows];
     __shared__ float sInv[kBulkRows];
     __shared__ int sCnt[kBulkRows];
+    __shared__ long long sOff[kBulkRows];   // element offset of the row in `out`; -1: none
     __shared__ volatile int sAbort;
-    ptx::wait_prior_grid();  // launched early (programmatic serialization): partials complete
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.y;
-    const int b = blockIdx.x / row_blocks;
-    const int pos0 = (blockIdx.x % row_blocks) * kBulkRows;
-    const SeqInfo si = seq_info(p, b);
-    if (pos0 >= si.sq) return;
-    const int nrows = min(kBulkRows, si.sq - pos0);
+    const int r0 = blockIdx.x * kBulkRows;
+    const int nrows = min(kBulkRows, p.total_q - r0);
     const int S = p.S;
-    const int64_t plane = (int64_t)p.total_q;
-    const int row0 = si.q0 + pos0;
+    const int64_t plane = p.total_q;
     const uint32_t bar = ptx::smem_u32(&sBar);
     const float *sO = (const float *)sO_raw;
-
     if (tid == 0) {
-        // the copies start first: the splits the block partition leaves non-empty for this
-        // M block bound every row's merged count (and are the ones the partial kernel wrote)
         sAbort = 0;
         ptx::mbar_init(bar, 1);
         ptx::fence_mbar_init();
-        const int ne = nonempty_splits(p, si.sq, si.last_valid, pos0);
+    }
+    ptx::wait_prior_grid();  // launched early (programmatic serialization): partials complete
+
+    if (tid == 0) {
         const uint32_t chunk = (uint32_t)nrows * DV * 4;
-        ptx::mbar_arrive_expect_tx(bar, chunk * (uint32_t)ne);
-        for (int sp = 0; sp < ne; ++sp)
+        ptx::mbar_arrive_expect_tx(bar, chunk * (uint32_t)S);
+        for (int sp = 0; sp < S; ++sp)
             ptx::bulk_load(ptx::smem_u32(sO_raw) + (uint32_t)sp * kBulkRows * DV * 4,
-                           o_part + (((int64_t)h * S + sp) * plane + row0) * DV, chunk, bar);
+                           o_part + (((int64_t)h * S + sp) * plane + r0) * DV, chunk, bar);
     }
     if (warp == 0 && lane < kBulkRows) {
-        // one lane per row: its merged count, then m = max(max_s L_s, lowest finite),
-        // w_s = exp(L_s - m)
         const int r = lane;
-        const int c = r < nrows
-                          ? merged_splits(p, si.sq, si.last_valid, pos0 + r, row_count(p, si, counts, pos0 + r))
-                          : 0;
-        sCnt[r] = c;
-        const float *lrow = lse_part + (int64_t)h * S * plane + row0 + r;
+        const bool row_in = r < nrows;
+        // the row's L_s first (in bounds for every s < S; only s < count are used)
+        const float *lrow = lse_part + (int64_t)h * S * plane + r0 + r;
         float l[kBulkMaxSplits];
+#pragma unroll
+        for (int sp = 0; sp < kBulkMaxSplits; ++sp)
+            l[sp] = (row_in && sp < S) ? __ldg(lrow + sp * plane) : -INFINITY;
+        int c = 0;
+        long long off = -1;
+        if (row_in) {
+            int pos = 0;
+            const int b = seq_of_row(p, r0 + r, &pos);
+            const SeqInfo si = seq_info(p, b);
+            if (pos >= 0 && pos < si.sq) {  // else a row outside every sequence: not written
+                c = merged_splits(p, si.sq, si.last_valid, pos, row_count(p, si, counts, pos));
+                off = row_offset(p, out, b, si.q0, pos);
+            }
+        }
+        sCnt[r] = c;
+        sOff[r] = off;
+        // m = max(max_s L_s, lowest finite), w_s = exp(L_s - m) over s < count
         float m = -FLT_MAX;
 #pragma unroll
-        for (int sp = 0; sp < kBulkMaxSplits; ++sp) {
-            l[sp] = sp < c ? __ldg(lrow + sp * plane) : -INFINITY;
-            m = fmaxf(m, l[sp]);
-        }
+        for (int sp = 0; sp < kBulkMaxSplits; ++sp)
+            if (sp < c) m = fmaxf(m, l[sp]);
         float wsum = 0.f;
 #pragma unroll
         for (int sp = 0; sp < kBulkMaxSplits; ++sp) {
@@ -236,18 +269,20 @@ __global__ void __launch_bounds__(kBulkThreads)
             wsum += w;
         }
         sInv[r] = 1.f / fmaxf(wsum, 1.f);  // the max only binds when every split is empty
-        if (lse_out && r < nrows)
-            lse_out[(int64_t)h * plane + row0 + r] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+        if (lse_out && off >= 0)
+            lse_out[(int64_t)h * plane + r0 + r] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
     }
     __syncthreads();
     if (!ptx::mbar_wait_bounded(bar, 0, &sAbort, p.err, 0x301, kBulkTimeoutNs)) return;
 #pragma unroll
-    for (int i = 0; i < kBulkRows / 4; ++i) {
-        const int r = warp * (kBulkRows / 4) + i;
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int r = warp * kRowsPerWarp + i;
         if (r >= nrows) break;  // warp-uniform
+        const long long off = sOff[r];
+        if (off < 0) continue;  // warp-uniform
         const int c = sCnt[r];
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane < kLanes) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int sp = 0; sp < c; ++sp) {
                 const float4 o = *(const float4 *)(sO + ((size_t)sp * kBulkRows + r) * DV + lane * 4);
                 const float w = sW[sp][r];
@@ -257,8 +292,7 @@ __global__ void __launch_bounds__(kBulkThreads)
                 acc.w = fmaf(w, o.w, acc.w);
             }
             const float inv = sInv[r];
-            TO *dst = (TO *)out.ptr + row_offset(p, out, b, si.q0, pos0 + r) + (int64_t)h * out.sh +
-                      lane * 4;
+            TO *dst = (TO *)out.ptr + off + (int64_t)h * out.sh + lane * 4;
             if constexpr (sizeof(TO) == 4) {
                 *(float4 *)dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             } else {
@@ -270,11 +304,11 @@ __global__ void __launch_bounds__(kBulkThreads)
     }
 }
 
-template <typename TO, int DV, int kBulkRows>
+template <typename TO, int DV>
 static cudaError_t launch_bulk(const Problem &p, const float *o_part, const float *lse_part,
                                const int32_t *counts, const TensorView &out, float *lse_out,
                                cudaStream_t st) {
-    auto kern = combine_bulk_kernel<TO, DV, kBulkRows>;
+    auto kern = combine_bulk_kernel<TO, DV>;
     constexpr int kMaxSmem = kBulkMaxSplits * kBulkRows * DV * 4;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -284,12 +318,10 @@ static cudaError_t launch_bulk(const Problem &p, const float *o_part, const floa
         attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
-    const int row_blocks = (p.max_sq + kBulkRows - 1) / kBulkRows;
-    const long long nx = (long long)row_blocks * p.B;
-    if (nx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int row_blocks = (p.total_q + kBulkRows - 1) / kBulkRows;
     const int smem = p.S * kBulkRows * DV * 4;
-    return launch_after_prior(kern, dim3((unsigned)nx, (unsigned)p.H), dim3(kBulkThreads), (size_t)smem, st,
-                              p, o_part, lse_part, counts, out, lse_out, row_blocks);
+    return launch_after_prior(kern, dim3((unsigned)row_blocks, (unsigned)p.H), dim3(kBulkThreads),
+                              (size_t)smem, st, p, o_part, lse_part, counts, out, lse_out);
 }
 
 template <typename TO>
@@ -298,8 +330,8 @@ static cudaError_t launch_dv(const Problem &p, const float *o_part, const float 
                              cudaStream_t st) {
     if (p.S > kMaxSplits) return cudaErrorInvalidValue;
     if (p.S <= kBulkMaxSplits) {
-        if (p.d_v == 128) return launch_bulk<TO, 128, kBulkRowsDefault>(p, o_part, lse_part, counts, out, lse_out, st);
-        if (p.d_v == 64) return launch_bulk<TO, 64, kBulkRowsDefault>(p, o_part, lse_part, counts, out, lse_out, st);
+        if (p.d_v == 128) return launch_bulk<TO, 128>(p, o_part, lse_part, counts, out, lse_out, st);
+        if (p.d_v == 64) return launch_bulk<TO, 64>(p, o_part, lse_part, counts, out, lse_out, st);
     }
     const int row_blocks = (p.max_sq + kRowsPerCta - 1) / kRowsPerCta;
     const long long nx = (long long)row_blocks * p.B;

@@ -130,3 +130,18 @@ def test_code_hash_ignores_comments_and_whitespace():
     c = "int f(int x) { return x + 2; }\n"
     assert bench.code_text(a) == bench.code_text(b)
     assert bench.code_text(b) != bench.code_text(c)
+
+
+def test_roofline_entry_reports_burst_and_sustained_fractions():
+    peaks = {"bf16": 1890.1, "bf16_sustained": 1692.7, "hbm": 6770.5, "source": "measured"}
+    w = wl.TARGET_SHAPE
+    fl = bench.flops_of(w)
+    loop = {"mean_ms": 0.8, "median_ms": 0.79, "launches": 1250, "seconds": 1.0}
+    r = bench.roofline_of(w, "partial_tc", fl, loop, peaks, None, {"sm_mhz": 2000})
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - fl / 0.8e-3 / 1e12) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / 1890.1) < 1e-12
+    assert abs(r["frac_sustained"] - r["achieved"] / 1692.7) < 1e-12
+    d = bench.roofline_of(wl.DECODE, "partial_tc", bench.flops_of(wl.DECODE), loop, peaks, None, {})
+    assert d["bound"] == "hbm" and d["unit"] == "GB/s"
+    assert abs(d["achieved"] - bench.kv_bytes_of(wl.DECODE) / 0.8e-3 / 1e9) < 1e-6

@@ -603,3 +603,4 @@ def test_fused_merge_matches_oracle_full_size():
     ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q.cpu(), k.cpu(), v.cpu(), rows=rows)
     out, lse, _ = H.run_fwd(w, q, k, v, DEV, fuse_combine=1)
     H.assert_close(H.to_np(out, rows), H.lse_np(lse, rows), ref_o, ref_l, w.dtype, "fused target")
+
