@@ -3,7 +3,8 @@
 
 namespace sk {
 
-// Tensor cores (tcgen05) for 16-bit storage with the library's M block (prefill and decode);
+// Tensor cores (tcgen05) for 16-bit storage with the library's M block (prefill and decode;
+// launches of many short units in the persistent form, one CTA per SM);
 // the streaming decode kernel for up to 16 queries per sequence where the tensor-core
 // kernel does not apply (other M blocks, more than 65535 (sequence, split) units, tensors
 // its TMA maps cannot describe); the CUDA-core kernel for the rest (f32 storage, other M
@@ -11,7 +12,7 @@ namespace sk {
 const char *partial_kernel_name(const Problem &p, int dtype, const TensorView &q,
                                 const TensorView &k, const TensorView &v) {
     (void)q; (void)k; (void)v;
-    if (tc::partial_tc_supported(p, dtype)) return "partial_tc";
+    if (tc::partial_tc_supported(p, dtype)) return tc::persist_selected(p) ? "partial_tc_persist" : "partial_tc";
     if (dec::partial_decode_supported(p, dtype)) return "partial_decode";
     return "partial_simt";
 }

@@ -678,6 +678,24 @@ bool partial_tc_supported(const Problem &p, int dtype) {
     return true;
 }
 
+// SM count of the current device (cached per device).
+static int sm_count_of_device() {
+    static int sms[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        sms[dev] = n;
+    }
+    return sms[dev];
+}
+
+bool persist_selected(const Problem &p) {
+    const int sms = sm_count_of_device();
+    return sms > 0 && persist_fits(p, sms);
+}
+
 cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, const TensorView &k,
                               const TensorView &v, float *o_part, float *lse_part,
                               const TensorView *out, float *lse_out, int *tickets, cudaStream_t st,
@@ -693,6 +711,10 @@ cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, 
         !make_map(&mv, v, dtype, p.d_v, krows, p.H, p.B, dense, p.d_qk == 192 ? 64 : 128))
         return cudaSuccess;  // not expressible as TMA maps: the caller falls back
     *launched = true;
+    // many short units: one CTA per SM takes them in turn (partial_tc_persist.cu)
+    if (!tickets && persist_selected(p))
+        return launch_partial_tc_persist(p, dtype, mq, mk, mv, o_part, lse_part, out, lse_out,
+                                         sm_count_of_device(), st);
 #define SK_TC_DIMS(T)                                                                              \
     if (p.d_qk == 192) return launch_dims<T, 192, 128>(p, mq, mk, mv, o_part, lse_part, out, lse_out, tickets, st); \
     if (p.d_qk == 128) return launch_dims<T, 128, 128>(p, mq, mk, mv, o_part, lse_part, out, lse_out, tickets, st); \

@@ -254,6 +254,14 @@ cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, 
                               const TensorView &v, float *o_part, float *lse_part,
                               const TensorView *out, float *lse_out, int *tickets, cudaStream_t st,
                               bool *launched);
+// The persistent form (partial_tc_persist.cu): whether it takes the launch, and the launch
+// with the tensor maps already made (out: split 1, the output written directly).
+bool persist_fits(const Problem &p, int sm_count);
+bool persist_selected(const Problem &p);  // persist_fits with the current device's SM count
+cudaError_t launch_partial_tc_persist(const Problem &p, int dtype, const CUtensorMap &mq,
+                                      const CUtensorMap &mk, const CUtensorMap &mv, float *o_part,
+                                      float *lse_part, const TensorView *out, float *lse_out,
+                                      int sm_count, cudaStream_t st);
 // TMA map of a [rows, H, D] (varlen) or [B][rows][H][D] (dense) 16-bit tensor: boxes of
 // 64 elements x box_rows rows, 128-byte swizzle. False when TMA cannot describe it.
 bool make_map(CUtensorMap *m, const TensorView &t, int dtype, int D, long long rows, int H, int B,

@@ -71,6 +71,8 @@ struct SoftmaxBars {
 // KVI (M blocks of at most 128 rows): both warpgroups own the same 128 rows, and tile t
 // takes the key tiles 2 i + t; the loop then hands back its m and l (base 2) instead of
 // writing anything, and kvi_epilogue merges the two halves.
+// A CTA that runs several units in turn (the persistent form) passes the number of S_t
+// phases its earlier units used (step0) and the parity of this unit's O-done phase.
 // Returns false when a wait gave up (the CTA's abort flag is then raised).
 template <typename T, int DV, bool DIRECT, bool KVI = false>
 __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si, int b, int h, int s,
@@ -79,7 +81,8 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
                                              volatile int *abort_flag, float *o_part,
                                              float *lse_part, const TensorView &out, float *lse_out,
                                              float4 *stage, float *m_out = nullptr,
-                                             float *l_out = nullptr) {
+                                             float *l_out = nullptr, uint32_t step0 = 0,
+                                             uint32_t o_phase = 0) {
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3;
@@ -98,7 +101,7 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
     bool ok = true;
     const int n_mine = KVI ? (n_tiles + 1 - t) / 2 : n_tiles;  // KVI: t = 0 even, t = 1 odd tiles
     for (int j = 0; j < n_mine; ++j) {
-        ok = warp_wait(bars.s_full, j & 1, abort_flag, p.err, kErrSoftmax);
+        ok = warp_wait(bars.s_full, (step0 + j) & 1, abort_flag, p.err, kErrSoftmax);
         if (!ok) break;
         ptx::tc_fence_after();
         uint32_t r[128];
@@ -161,7 +164,7 @@ __device__ __forceinline__ bool softmax_rows(const Problem &p, const SeqInfo &si
         ptx::tc_fence_before();
         ptx::mbar_arrive(bars.p_ready);
     }
-    if (ok && n_tiles > 0) ok = warp_wait(bars.o_done, 0, abort_flag, p.err, kErrSoftmax);
+    if (ok && n_tiles > 0) ok = warp_wait(bars.o_done, o_phase, abort_flag, p.err, kErrSoftmax);
     if constexpr (KVI) {
         *m_out = m;
         *l_out = l;

@@ -604,3 +604,65 @@ def test_fused_merge_matches_oracle_full_size():
     out, lse, _ = H.run_fwd(w, q, k, v, DEV, fuse_combine=1)
     H.assert_close(H.to_np(out, rows), H.lse_np(lse, rows), ref_o, ref_l, w.dtype, "fused target")
 
+
+# ------------------------------------------------- the persistent tensor-core form
+#
+# Launches of more (sequence, head, split, M block) units than SMs, each with a few key
+# tiles, run on partial_tc_persist: one CTA per SM takes the units in turn. Each case
+# below is shaped to land there (checked through sk_partial_kernel_name) and compared with
+# the oracle: the partials of sk_attn_partial_fwd (empty splits write 0 / -inf), the
+# one-call forward (empty splits write nothing) and the three-call path.
+
+PERSIST = [
+    wl.Workload("persist causal bf16 D128 S8", H=8, seqlens_q=(600, 300, 513),
+                seqlens_k=(700, 1200, 600), d_qk=128, d_v=128, dtype="bf16", seed=41,
+                n_per_block=64, split_kv=8, mask=wl.MASK_CAUSAL),
+    wl.Workload("persist prefix window f16 D64 S5", H=12, seqlens_q=(700, 257),
+                seqlens_k=(2000, 900), d_qk=64, d_v=64, dtype="f16", seed=42, n_per_block=32,
+                split_kv=5, mask=wl.MASK_PREFIX_CAUSAL, prefix_offset=300, window_left=400),
+    wl.Workload("persist non-causal bf16 D128 padded lastValid S6", H=10,
+                seqlens_q=(520, 300, 130), seqlens_k=(1500, 3000, 200), d_qk=128, d_v=128,
+                dtype="bf16", seed=43, n_per_block=128, split_kv=6, last_valid_kv_index=2000,
+                seqused_k=(1400, 2500, 0)),
+    wl.Workload("persist causal bf16 D128 split 1", H=16, seqlens_q=(513, 300, 260, 400),
+                seqlens_k=(1000, 800, 1500, 2000), d_qk=128, d_v=128, dtype="bf16", seed=44,
+                n_per_block=128, split_kv=1, mask=wl.MASK_CAUSAL),
+    wl.Workload("persist prefix -100 f16 D128 S4", H=16, seqlens_q=(1024,), seqlens_k=(1024,),
+                d_qk=128, d_v=128, dtype="f16", seed=45, n_per_block=64, split_kv=4,
+                mask=wl.MASK_PREFIX_CAUSAL, prefix_offset=-100),
+]
+
+
+@pytest.mark.parametrize("w", PERSIST, ids=lambda w: w.name)
+def test_persistent_form_matches_oracle(w):
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    S = w.split_kv
+    p = skv.params_for(w, DEV)
+    assert skv.sk_partial_kernel_name(p, qd, kd, vd) == "partial_tc_persist"
+    o_part, l_part, _ = H.run_partials(w, qd, kd, vd, DEV, S)
+    ref_po, ref_pl = oracle.partials(H.oracle_problem(w, S), q, k, v)
+    got_o = o_part.permute(2, 0, 1, 3).cpu().numpy()
+    got_l = l_part.permute(2, 0, 1).cpu().numpy()
+    H.assert_close(got_o, got_l, ref_po, ref_pl, w.dtype, "persistent partials")
+    empty = np.isneginf(ref_pl)
+    assert (got_o[empty] == 0).all() and np.isneginf(got_l[empty]).all()
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "persistent forward")
+    out3, lse3 = _three_call(w, qd, kd, vd, S)
+    H.assert_close(H.to_np(out3), H.lse_np(lse3), ref_o, ref_l, w.dtype, "persistent three calls")
+
+
+def test_persistent_form_on_the_masked_workload_full_size():
+    """The masked f16 workload (512 units of one to four key tiles) runs on the persistent
+    form; sampled rows of every mask variant against the oracle."""
+    w = wl.MASKED_F16
+    q, k, v = w.make_inputs(DEV)
+    assert skv.sk_partial_kernel_name(skv.params_for(w, DEV), q, k, v) == "partial_tc_persist"
+    for mask, po in ((wl.MASK_CAUSAL, 0), (wl.MASK_PREFIX_CAUSAL, 2048), (wl.MASK_PREFIX_CAUSAL, -256)):
+        wm = w.with_(mask=mask, prefix_offset=po)
+        rows = H.sample_rows(wm, head=64, tail=64, rand=64)
+        ref_o, ref_l = oracle.attention(H.oracle_problem(wm, 1), q.cpu(), k.cpu(), v.cpu(), rows=rows)
+        out, lse, _ = H.run_fwd(wm, q, k, v, DEV)
+        H.assert_close(H.to_np(out, rows), H.lse_np(lse, rows), ref_o, ref_l, wm.dtype,
+                       f"masked persistent po={po}")
