@@ -455,10 +455,50 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     if launches_per_step == 1 and not fused:
         roof["note"] = "split 1: a step is this kernel writing the output directly"
 
-    # end to end through the public call: every step copies its Q, K, V in from pinned
-    # host memory and its output back out. Two device buffer sets let step i + 1's inputs
-    # and step i's output travel on their own streams while steps compute in order on the
-    # compute stream (the copies stay inside the timed region).
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_block(skv, p, q, k, v, out, ws, w, world, fl, stream, dev, args)
+    ms = max_over_ranks([ms], device=dev if dist_on else None)[0]
+    varlen = None
+    if world == 1 and args.workload != "varlen" and not args.no_varlen:
+        del q, k, v, ws, out
+        torch.cuda.empty_cache()
+        varlen = varlen_block(skv, args, peaks, dev, stream)
+    if rank != 0:
+        return None
+
+    line = {
+        "metric": METRIC, "value": whole_job_tflops(fl, world, ms), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": vs_pages(args.workload, whole_job_tflops(fl, world, ms)),
+        "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+        "config": {**shape_config(w),
+                   "split_kv": S, "fuse_combine": p.fuse_combine,
+                   "block_m": skv.sk_default_block_m(w.d_qk, w.d_v),
+                   "l2": "inputs larger than L2 "
+                   f"({(w.total_q * w.d_qk + w.total_k * (w.d_qk + w.d_v)) * w.H * (4 if w.dtype == 'f32' else 2) / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "combine": comb,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if varlen is not None:
+        line["varlen"] = varlen
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(w, args.cpu_seconds)
+    return line
+
+
+def e2e_block(skv, p, q, k, v, out, ws, w, world, fl, stream, dev, args) -> dict:
+    """The step end to end through the public call with host buffers.
+
+    Every step copies its Q, K, V in from pinned host memory and its output back out. Two
+    device buffer sets let step i + 1's inputs and step i's output travel on their own
+    streams while steps compute in order on the compute stream (the copies stay inside the
+    timed region)."""
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     bufs = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out))
@@ -501,51 +541,20 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     e2e_run(3)
     torch.cuda.synchronize()
     n_e2e = max(args.steps // 4, 5)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     e2e_run(n_e2e)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
-    del hq, hk, hv, hout, bufs
-
-    ms, e2e_ms = max_over_ranks([ms, e2e_ms], device=dev if dist_on else None)
-    varlen = None
-    if world == 1 and args.workload != "varlen" and not args.no_varlen:
-        del q, k, v, ws, out
-        torch.cuda.empty_cache()
-        varlen = varlen_block(skv, args, peaks, dev, stream)
-    if rank != 0:
-        return None
-
-    line = {
-        "metric": METRIC, "value": whole_job_tflops(fl, world, ms), "unit": UNIT,
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": vs_pages(args.workload, whole_job_tflops(fl, world, ms)),
-        "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
-        "config": {**shape_config(w),
-                   "split_kv": S, "fuse_combine": p.fuse_combine,
-                   "block_m": skv.sk_default_block_m(w.d_qk, w.d_v),
-                   "l2": "inputs larger than L2 "
-                   f"({(w.total_q * w.d_qk + w.total_k * (w.d_qk + w.d_v)) * w.H * (4 if w.dtype == 'f32' else 2) / 1e6:.0f} MB)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roof,
-        "combine": comb,
-        "e2e": {"value": whole_job_tflops(fl, world, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": int(w.H * (w.total_q * w.d_qk + w.total_k * (w.d_qk + w.d_v))
-                                          * (4 if w.dtype == "f32" else 2)),
-                "d2h_bytes_per_step": int(w.total_q * w.H * w.d_v * (4 if w.dtype == "f32" else 2)),
-                "ms_per_step": e2e_ms,
-                "overlap": "step i+1's host-to-device copies and step i's read-back run on their "
-                           "own streams beside step i's compute"},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
-    }
-    if varlen is not None:
-        line["varlen"] = varlen
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = time_oracle(w, args.cpu_seconds)
-    return line
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / n_e2e],
+                            device=dev if torch.distributed.is_initialized() else None)[0]
+    h2d_bytes = int(sum(t.numel() * t.element_size() for t in (q, k, v)))
+    return {"value": whole_job_tflops(fl, world, e2e_ms), "unit": UNIT,
+            "h2d_bytes_per_step": h2d_bytes,
+            "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+            "ms_per_step": e2e_ms,
+            "overlap": "step i+1's host-to-device copies and step i's read-back run on their "
+                       "own streams beside step i's compute"}
 
 
 def varlen_block(skv, args, peaks: dict, dev, stream) -> dict:
@@ -624,6 +633,8 @@ def main():
                     help="device time of each kernel-alone loop (partial kernel, combine)")
     ap.add_argument("--no-varlen", action="store_true",
                     help="skip the long-context varlen block of the JSON line")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--step-only", action="store_true",
                     help="time the steps only (no kernel loops, end-to-end, varlen block or CPU "
                          "baseline): the command the profiler captures")
