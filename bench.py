@@ -10,9 +10,9 @@ Prints one JSON line. Besides the step throughput it reports, measured live:
                 the measured dense bf16 peak, plus ncu DRAM traffic from profiles/
   combine       the combine kernel's HBM GB/s (back-to-back launches over rotating copies of
                 the partials that together exceed L2 three times)
-  e2e           the same metric through the public call with host buffers and
-                host<->device copies inside the timed region (each step's copies overlap
-                the neighbouring steps' compute, two device buffer sets)
+  e2e           the same metric through the library's host-buffer call (sk_attn_fwd_host),
+                host<->device copies inside the timed region (steps alternate between two
+                streams, so one step's copies overlap the other's compute)
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
   clocks        nvidia-smi samples taken during the timed work
 
@@ -493,68 +493,43 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
 
 
 def e2e_block(skv, p, q, k, v, out, ws, w, world, fl, stream, dev, args) -> dict:
-    """The step end to end through the public call with host buffers.
-
-    Every step copies its Q, K, V in from pinned host memory and its output back out. Two
-    device buffer sets let step i + 1's inputs and step i's output travel on their own
-    streams while steps compute in order on the compute stream (the copies stay inside the
-    timed region)."""
+    """The step end to end through the library's host-buffer call, sk_attn_fwd_host: every step
+    copies its Q, K, V in from pinned host memory, runs the forward pass and copies its output
+    back, all enqueued by the one call. Steps alternate between two streams with a device buffer
+    each, so that one step's copies overlap the other's compute."""
+    code = {"bf16": skv.SK_BF16, "f16": skv.SK_F16, "f32": skv.SK_F32}[w.dtype]
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    bufs = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out))
-            for _ in range(2)]
-    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    copied = [torch.cuda.Event() for _ in range(2)]
-    computed = [torch.cuda.Event() for _ in range(2)]
-    drained = [torch.cuda.Event() for _ in range(2)]
+    nbytes = skv.sk_host_buffer_bytes(p, code, False)
+    bufs = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
 
-    def e2e_run(n_steps):
+    def run(n_steps):
         start = torch.cuda.Event()
         start.record(stream)
-        h2d.wait_event(start)
-
-        def issue_h2d(i):
-            b = i % 2
-            if i >= 2:
-                h2d.wait_event(computed[b])   # step i - 2 is done with this set's inputs
-            with torch.cuda.stream(h2d):
-                for dst, src in zip(bufs[b][:3], (hq, hk, hv)):
-                    dst.copy_(src, non_blocking=True)
-                copied[b].record(h2d)
-
-        issue_h2d(0)
+        for st in streams:
+            st.wait_event(start)
         for i in range(n_steps):
-            b = i % 2
-            if i + 1 < n_steps:
-                issue_h2d(i + 1)
-            stream.wait_event(copied[b])
-            if i >= 2:
-                stream.wait_event(drained[b])  # step i - 2's output has been read back
-            skv.sk_attn_fwd(p, bufs[b][0], bufs[b][1], bufs[b][2], bufs[b][3], None, ws)
-            computed[b].record(stream)
-            d2h.wait_event(computed[b])
-            with torch.cuda.stream(d2h):
-                hout[b].copy_(bufs[b][3], non_blocking=True)
-                drained[b].record(d2h)
-        stream.wait_stream(d2h)
+            skv.sk_attn_fwd_host(p, hq, hk, hv, hout[i % 2], None, bufs[i % 2], stream=streams[i % 2])
+        for st in streams:
+            stream.wait_stream(st)
 
-    e2e_run(3)
+    run(3)
     torch.cuda.synchronize()
     n_e2e = max(args.steps // 4, 5)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    e2e_run(n_e2e)
+    run(n_e2e)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks([e0.elapsed_time(e1) / n_e2e],
                             device=dev if torch.distributed.is_initialized() else None)[0]
-    h2d_bytes = int(sum(t.numel() * t.element_size() for t in (q, k, v)))
+    h2d_bytes = int(sum(t.numel() * t.element_size() for t in (hq, hk, hv)))
     return {"value": whole_job_tflops(fl, world, e2e_ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d_bytes,
-            "d2h_bytes_per_step": int(out.numel() * out.element_size()),
-            "ms_per_step": e2e_ms,
-            "overlap": "step i+1's host-to-device copies and step i's read-back run on their "
-                       "own streams beside step i's compute"}
+            "d2h_bytes_per_step": int(hout[0].numel() * hout[0].element_size()),
+            "ms_per_step": e2e_ms, "call": "sk_attn_fwd_host",
+            "overlap": "steps alternate between two streams, each with its own device buffer"}
 
 
 def varlen_block(skv, args, peaks: dict, dev, stream) -> dict:

@@ -197,6 +197,32 @@ sk_status sk_attn_fwd(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
 sk_status sk_attn_fwd_static(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
                              sk_tensor out, float *lse_out, sk_stream stream);
 
+/*
+ * sk_attn_fwd_host -- sk_attn_fwd with Q, K, V and the output in HOST memory, for callers whose
+ * data lives on the host (the one-call form of the pages' varlen API, with the copies inside).
+ *   - q, k, v, out: host pointers to contiguous tensors, [total, H, d] packed (stride_row =
+ *     H * d, stride_h = d) or [B, seq, H, d] dense (stride_b = seq * H * d); any other
+ *     strides return SK_ERR_UNSUPPORTED. All four have the same storage type.
+ *   - lse_out: host float [H][total_q], or NULL.
+ *   - cu_seqlens_q / cu_seqlens_k / seqused_k in p stay DEVICE pointers, as in every call.
+ *   - device_buffer: caller-owned device memory, 256-byte aligned, at least
+ *     sk_host_buffer_bytes() (SK_ERR_WORKSPACE otherwise): it holds device copies of Q, K,
+ *     V, the output and the LSE, then sk_attn_fwd's workspace.
+ * Enqueued on `stream`, in order: the host-to-device copies of q, k, v, sk_attn_fwd on the
+ * device copies, the device-to-host copies of out (and lse_out). The call returns without
+ * waiting; the host output is complete once the stream has passed this point. With page-
+ * locked (pinned) host memory every copy is asynchronous; pageable host memory works, but
+ * its copies may return only once staged. Two calls on two streams with two device buffers
+ * overlap one call's copies with the other's compute. Nothing is allocated.
+ */
+sk_status sk_attn_fwd_host(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v,
+                           sk_tensor out, float *lse_out, void *device_buffer,
+                           size_t device_bytes, sk_stream stream);
+
+/* Bytes of device memory sk_attn_fwd_host needs for these parameters, storage type and
+ * whether an LSE is returned (with_lse 0 or 1). */
+sk_status sk_host_buffer_bytes(const sk_params *p, sk_dtype dtype, int with_lse, size_t *bytes);
+
 /* Bytes of workspace sk_attn_fwd needs for these parameters (0 when S == 1).
  * Resolving split_kv = 0 reads the current device's SM count. */
 sk_status sk_workspace_bytes(const sk_params *p, size_t *bytes);

@@ -5,7 +5,7 @@ computation runs in the library's CUDA kernels. PyTorch is used only for device
 memory and streams. The functions keep the C names:
 
   sk_valid_split_counts, sk_attn_partial_fwd, sk_combine, sk_attn_fwd,
-  sk_attn_fwd_static, sk_workspace_bytes, sk_auto_split_kv, sk_choose_split_kv,
+  sk_attn_fwd_static, sk_attn_fwd_host, sk_host_buffer_bytes, sk_workspace_bytes, sk_auto_split_kv, sk_choose_split_kv,
   sk_default_block_m, sk_partial_kernel_name, sk_status_string, sk_last_cuda_error,
   sk_selftest_bounded_wait, sk_read_device_error
 
@@ -259,6 +259,27 @@ def sk_attn_fwd_static(p: Params, q, k, v, out, lse_out=None, stream=None):
                    ctypes.c_void_p]
     _ok(fn(ctypes.byref(p.c()), tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out),
            _ptr(lse_out), _stream(stream)), "sk_attn_fwd_static")
+
+
+def sk_host_buffer_bytes(p: Params, dtype: int, with_lse: bool) -> int:
+    fn = lib().sk_host_buffer_bytes
+    fn.argtypes = [ctypes.POINTER(_Params), ctypes.c_int, ctypes.c_int,
+                   ctypes.POINTER(ctypes.c_size_t)]
+    out = ctypes.c_size_t()
+    _ok(fn(ctypes.byref(p.c()), dtype, int(with_lse), ctypes.byref(out)), "sk_host_buffer_bytes")
+    return out.value
+
+
+def sk_attn_fwd_host(p: Params, q, k, v, out, lse_out=None, device_buffer=None, stream=None):
+    """sk_attn_fwd with q, k, v, out (and lse_out) in host memory (contiguous CPU tensors,
+    pinned for asynchronous copies); device_buffer is a device uint8 tensor of at least
+    sk_host_buffer_bytes() bytes."""
+    fn = lib().sk_attn_fwd_host
+    fn.argtypes = [ctypes.POINTER(_Params), _Tensor, _Tensor, _Tensor, _Tensor, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    nbytes = 0 if device_buffer is None else device_buffer.numel() * device_buffer.element_size()
+    _ok(fn(ctypes.byref(p.c()), tensor_desc(q), tensor_desc(k), tensor_desc(v), tensor_desc(out),
+           _ptr(lse_out), _ptr(device_buffer), nbytes, _stream(stream)), "sk_attn_fwd_host")
 
 
 def sk_last_cuda_error() -> tuple[int, str]:

@@ -55,6 +55,14 @@ int main(void) {
     CHECK(sk_workspace_bytes(&p, &bytes) == SK_OK);
     CHECK(bytes == a256((size_t)12 * 3 * 4096 * 128 * 4) + a256((size_t)12 * 3 * 4096 * 4) +
                        a256((size_t)1 * 12 * 16 * 4));
+    /* the host-buffer call's device buffer: Q | K | V | out | LSE | workspace */
+    {
+        size_t ws = bytes, host = 0;
+        CHECK(sk_host_buffer_bytes(&p, SK_BF16, 1, &host) == SK_OK);
+        CHECK(host == a256((size_t)4096 * 12 * 192 * 2) + a256((size_t)42700 * 12 * 192 * 2) +
+                          a256((size_t)42700 * 12 * 128 * 2) + a256((size_t)4096 * 12 * 128 * 2) +
+                          a256((size_t)12 * 4096 * 4) + a256(ws));
+    }
     p.split_kv = 1;
     CHECK(sk_workspace_bytes(&p, &bytes) == SK_OK && bytes == 0);
 

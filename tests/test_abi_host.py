@@ -190,3 +190,40 @@ def test_status_strings(L):
     assert "unknown" in skv.sk_status_string(99)
     assert L.sk_version() >= 100
     assert L.sk_supported_head_dims(192, 128) and not L.sk_supported_head_dims(192, 192)
+
+
+def _host_fwd(L, p, q=None, k=None, v=None, out=None, buf=FAKE, nbytes=1 << 40):
+    fn = L.sk_attn_fwd_host
+    fn.argtypes = [ctypes.POINTER(skv._Params), skv._Tensor, skv._Tensor, skv._Tensor, skv._Tensor,
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    q, k, v, out = q or _t(), k or _t(), v or _t(), out or _t()
+    return fn(ctypes.byref(p.c()), q, k, v, out, None, buf, nbytes, None)
+
+
+def test_host_entry_buffer_layout(L):
+    def a256(x):
+        return (x + 255) // 256 * 256
+    p = _params(split_kv=3)
+    ws = skv.sk_workspace_bytes(p)
+    es = 2
+    q, kk = p.total_q * p.H * p.d_qk * es, p.total_k * p.H * p.d_qk * es
+    v, o, lse = p.total_k * p.H * p.d_v * es, p.total_q * p.H * p.d_v * es, p.H * p.total_q * 4
+    assert skv.sk_host_buffer_bytes(p, skv.SK_BF16, True) == (a256(q) + a256(kk) + a256(v) + a256(o)
+                                                              + a256(lse) + a256(ws))
+    assert skv.sk_host_buffer_bytes(p, skv.SK_BF16, False) == (a256(q) + a256(kk) + a256(v) + a256(o)
+                                                               + a256(ws))
+    assert (skv.sk_host_buffer_bytes(p, skv.SK_F32, False) - a256(ws)
+            == a256(2 * q) + a256(2 * kk) + a256(2 * v) + a256(2 * o))
+
+
+def test_host_entry_rejected_before_any_copy(L):
+    p = _params(split_kv=3)
+    need = skv.sk_host_buffer_bytes(p, skv.SK_BF16, False)
+    assert _host_fwd(L, p, q=_t(ptr=0)) == SK_ERR_INVALID_ARG                 # null host tensor
+    assert _host_fwd(L, p, k=_t(sr=1024)) == SK_ERR_UNSUPPORTED               # rows not packed
+    assert _host_fwd(L, p, v=_t(sh=256, sr=1024)) == SK_ERR_UNSUPPORTED       # heads not packed
+    assert _host_fwd(L, p, out=_t(dtype=skv.SK_F16)) == SK_ERR_UNSUPPORTED    # mixed storage types
+    assert _host_fwd(L, p, nbytes=need - 1) == SK_ERR_WORKSPACE
+    assert _host_fwd(L, p, buf=FAKE + 16, nbytes=need) == SK_ERR_INVALID_ARG  # not 256-byte aligned
+    assert _host_fwd(L, p, buf=0, nbytes=need) == SK_ERR_INVALID_ARG
+    assert _host_fwd(L, _params(B=0)) == SK_ERR_INVALID_ARG

@@ -666,3 +666,25 @@ def test_persistent_form_on_the_masked_workload_full_size():
         out, lse, _ = H.run_fwd(wm, q, k, v, DEV)
         H.assert_close(H.to_np(out, rows), H.lse_np(lse, rows), ref_o, ref_l, wm.dtype,
                        f"masked persistent po={po}")
+
+
+@pytest.mark.parametrize("S,mask,heads,sq", [(8, wl.MASK_CAUSAL, 16, 300), (1, wl.MASK_NONE, 32, 600)])
+def test_persistent_form_dense_layout_equals_varlen(S, mask, heads, sq):
+    """[B, seq, H, D] tensors without cu_seqlens on the persistent form (partials and, at split 1,
+    the output written directly) give the packed layout's results bit for bit."""
+    w = wl.Workload("dense persistent", H=heads, seqlens_q=(sq, sq), seqlens_k=(1600, 1600),
+                    d_qk=128, d_v=128, dtype="bf16", seed=46, n_per_block=128, split_kv=S,
+                    mask=mask)
+    (_, _, _), (qd, kd, vd) = _inputs(w)
+    p = skv.params_for(w, DEV)
+    assert skv.sk_partial_kernel_name(p, qd, kd, vd) == "partial_tc_persist"
+    out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
+    p.cu_seqlens_q = p.cu_seqlens_k = None
+    qb, kb, vb = (t.view(2, -1, heads, 128) for t in (qd, kd, vd))
+    outb = torch.empty(2, sq, heads, 128, dtype=qd.dtype, device=DEV)
+    lseb = torch.empty(heads, 2 * sq, dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(skv.sk_workspace_bytes(p), 1), dtype=torch.uint8, device=DEV)
+    assert skv.sk_partial_kernel_name(p, qb, kb, vb) == "partial_tc_persist"
+    skv.sk_attn_fwd(p, qb, kb, vb, outb, lseb, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(outb.view_as(out), out) and torch.equal(lseb, lse)
