@@ -7,14 +7,14 @@ namespace sk {
 // launches of many short units in the persistent form, one CTA per SM);
 // the streaming decode kernel for up to 16 queries per sequence where the tensor-core
 // kernel does not apply (other M blocks, more than 65535 (sequence, split) units, tensors
-// its TMA maps cannot describe); the CUDA-core kernel for the rest (f32 storage, other M
-// blocks, no keys).
+// its TMA maps cannot describe); the register-tiled CUDA-core kernel for the rest (f32 storage,
+// other M blocks, no keys).
 const char *partial_kernel_name(const Problem &p, int dtype, const TensorView &q,
                                 const TensorView &k, const TensorView &v) {
     (void)q; (void)k; (void)v;
     if (tc::partial_tc_supported(p, dtype)) return tc::persist_selected(p) ? "partial_tc_persist" : "partial_tc";
     if (dec::partial_decode_supported(p, dtype)) return "partial_decode";
-    return "partial_simt";
+    return "partial_fma";
 }
 
 cudaError_t run_partial(const Problem &p, int dtype, const TensorView &q, const TensorView &k,
@@ -32,7 +32,7 @@ cudaError_t run_partial(const Problem &p, int dtype, const TensorView &q, const 
                                                    st, &launched);
         if (launched || e != cudaSuccess) return e;
     }
-    return launch_partial_simt(p, dtype, q, k, v, o_part, lse_part, out, lse_out, st);
+    return launch_partial_fma(p, dtype, q, k, v, o_part, lse_part, out, lse_out, st);
 }
 
 cudaError_t run_partial_fused(const Problem &p, int dtype, const TensorView &q,

@@ -39,6 +39,7 @@
 //     TMA loads and MMAs, frees TMEM and returns.
 #include <float.h>
 
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -678,17 +679,24 @@ bool partial_tc_supported(const Problem &p, int dtype) {
     return true;
 }
 
-// SM count of the current device (cached per device).
+// SM count of the current device (cached per device; 0 when it cannot be read).
 static int sm_count_of_device() {
-    static int sms[64];
+    static std::atomic<int> sms[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (sms[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        sms[dev] = n;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
     }
-    return sms[dev];
+    if (dev < 0 || dev >= 64) return 0;
+    int n = sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        sms[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
 }
 
 bool persist_selected(const Problem &p) {

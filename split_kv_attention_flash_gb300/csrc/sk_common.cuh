@@ -244,10 +244,10 @@ template <int W> __device__ __forceinline__ float group_sum(float x) {
 // Launchers implemented in the .cu files (host side).
 namespace sk {
 cudaError_t launch_counts(const Problem &p, int32_t *counts, cudaStream_t st);
-cudaError_t launch_partial_simt(const Problem &p, int dtype, const TensorView &q,
-                                const TensorView &k, const TensorView &v, float *o_part,
-                                float *lse_part, const TensorView *out, float *lse_out,
-                                cudaStream_t st);
+cudaError_t launch_partial_fma(const Problem &p, int dtype, const TensorView &q,
+                               const TensorView &k, const TensorView &v, float *o_part,
+                               float *lse_part, const TensorView *out, float *lse_out,
+                               cudaStream_t st);
 namespace tc {
 bool partial_tc_supported(const Problem &p, int dtype);
 cudaError_t launch_partial_tc(const Problem &p, int dtype, const TensorView &q, const TensorView &k,

@@ -688,3 +688,33 @@ def test_persistent_form_dense_layout_equals_varlen(S, mask, heads, sq):
     skv.sk_attn_fwd(p, qb, kb, vb, outb, lseb, ws)
     torch.cuda.synchronize()
     assert torch.equal(outb.view_as(out), out) and torch.equal(lseb, lse)
+
+
+@pytest.mark.parametrize("dtype,dqk,dv,mask,po,window", [
+    ("bf16", 192, 128, wl.MASK_CAUSAL, 0, -1),
+    ("f16", 128, 128, wl.MASK_PREFIX_CAUSAL, 300, 150),
+    ("bf16", 64, 64, wl.MASK_NONE, 0, -1),
+])
+def test_cuda_core_kernel_for_other_m_blocks(dtype, dqk, dv, mask, po, window):
+    """16-bit storage with an M block of 64 rows and more than 16 queries per sequence: neither
+    tensor-core kernel nor the decode kernel applies, so the register-tiled CUDA-core kernel
+    computes the partials (compared under the same partition) and the output."""
+    w = _small(dtype, dqk, dv, mask=mask, po=po, S=3, bn=64, sq=(300, 1, 77, 200),
+               sk=(1000, 5, 0, 513), window=window)
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    bm = 64
+    p = skv.params_for(w, DEV, split_kv=3, block_m=bm)
+    assert skv.sk_partial_kernel_name(p, qd, kd, vd) == "partial_fma"
+    o_part = torch.empty(w.H, 3, w.total_q, w.d_v, dtype=torch.float32, device=DEV)
+    l_part = torch.empty(w.H, 3, w.total_q, dtype=torch.float32, device=DEV)
+    skv.sk_attn_partial_fwd(p, qd, kd, vd, o_part, l_part)
+    out = torch.empty(w.total_q, w.H, w.d_v, dtype=qd.dtype, device=DEV)
+    lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(skv.sk_workspace_bytes(p), 1), dtype=torch.uint8, device=DEV)
+    skv.sk_attn_fwd(p, qd, kd, vd, out, lse, ws)
+    torch.cuda.synchronize()
+    ref_po, ref_pl = oracle.partials(H.oracle_problem(w, 3, block_m=bm), q, k, v)
+    H.assert_close(o_part.permute(2, 0, 1, 3).cpu().numpy(), l_part.permute(2, 0, 1).cpu().numpy(),
+                   ref_po, ref_pl, w.dtype, "partials")
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
