@@ -718,3 +718,44 @@ def test_cuda_core_kernel_for_other_m_blocks(dtype, dqk, dv, mask, po, window):
                    ref_po, ref_pl, w.dtype, "partials")
     ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
     H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, "forward")
+
+
+def _random_workload(seed: int) -> wl.Workload:
+    """A seeded random small problem: 1-5 sequences of 0-700 queries and 0-1500 keys, every
+    head-dim pair and storage type, any mask with a random offset, window, lastValid, padded
+    key slots, key tile and split count."""
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 6))
+    sq = tuple(int(x) for x in rng.integers(0, 701, B))
+    if sum(sq) == 0:
+        sq = (1,) + sq[1:]
+    sk = tuple(int(x) for x in rng.integers(0, 1501, B))
+    dqk, dv = [(64, 64), (128, 128), (192, 128)][int(rng.integers(0, 3))]
+    dtype = ["bf16", "f16", "f32"][int(rng.integers(0, 3))]
+    mask = int(rng.integers(0, 3))
+    po = int(rng.integers(-300, 1500)) if mask == wl.MASK_PREFIX_CAUSAL else 0
+    window = int(rng.integers(0, 800)) if mask != wl.MASK_NONE and rng.random() < 0.4 else -1
+    lvi = int(rng.integers(0, 1500)) if rng.random() < 0.3 else -1
+    used = tuple(int(min(x, y)) for x, y in zip(sk, rng.integers(0, 1600, B))) if rng.random() < 0.3 else None
+    bn = int(rng.choice([16, 32, 64, 128, 256]))
+    S = int(rng.choice([1, 2, 3, 4, 5, 8, 13, 32]))
+    return wl.Workload(f"random {seed}", H=int(rng.integers(1, 5)), seqlens_q=sq, seqlens_k=sk,
+                       d_qk=dqk, d_v=dv, dtype=dtype, seed=seed, n_per_block=bn, split_kv=S,
+                       mask=mask, prefix_offset=po, last_valid_kv_index=lvi, window_left=window,
+                       seqused_k=used)
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_problems_match_oracle(seed):
+    """Seeded random problems through sk_attn_fwd (and its split counts) against the oracle."""
+    w = _random_workload(seed)
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    if w.total_k == 0:   # K and V need a real buffer even when no sequence has a key
+        kd = torch.zeros(1, w.H, w.d_qk, dtype=qd.dtype, device=DEV)
+        vd = torch.zeros(1, w.H, w.d_v, dtype=qd.dtype, device=DEV)
+    out, lse, p = H.run_fwd(w, qd, kd, vd, DEV)
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v)
+    H.assert_close(H.to_np(out), H.lse_np(lse), ref_o, ref_l, w.dtype, w.name)
+    counts = torch.empty(w.total_q, dtype=torch.int32, device=DEV)
+    skv.sk_valid_split_counts(p, counts)
+    assert np.array_equal(counts.cpu().numpy(), oracle.split_counts(H.oracle_problem(w, w.split_kv)))
