@@ -9,20 +9,13 @@
 // The pass is HBM-bound: it reads count * (4 d_v + 4) bytes and writes d_v
 // storage-type elements (+ 4 bytes of LSE) per (head, row).
 //
-// combine_bulk_kernel (S <= 8): a CTA merges 16 consecutive packed rows of one head,
-// whichever sequences they belong to. For a (head, split) plane those rows are one
-// contiguous chunk of 16 * d_v floats, so one thread first issues one bulk asynchronous
-// copy per split into shared memory, before any load the copies would depend on; warp 0
-// finds each row's sequence, count and weights while they land; then every warp merges
-// 4 rows out of shared memory.
-//
-// combine_kernel (any S <= 32): a CTA merges 32 consecutive rows of one head:
-//   * every warp reads the counts of its 4 rows and at once issues the 16-byte
-//     loads of up to kPrefetch partial rows each, so that a lane has up to 16
-//     independent loads in flight before any arithmetic;
-//   * meanwhile warp 0 (one lane per row) reads the L_s, forms m and the weights
-//     into shared memory and writes the final LSE, all coalesced;
-//   * after one barrier every warp weights, sums, scales and stores its rows.
+// combine_bulk_kernel: a CTA merges ROWS consecutive packed rows of one head, whichever
+// sequences they belong to: 16 rows for up to 8 splits, 8 for up to 16, 4 for up to 32, so
+// that the staged partials take at most 64 KB of shared memory. For a (head, split) plane
+// those rows are one contiguous chunk of ROWS * d_v floats, so one thread first issues one
+// bulk asynchronous copy per split into shared memory, before any load the copies would
+// depend on; warp 0 loads each row's log-sum-exps and finds its sequence, count and weights
+// while they land; then every warp merges its rows out of shared memory.
 #include <float.h>
 
 #include <mutex>
@@ -31,119 +24,6 @@
 #include "sm100_ptx.cuh"
 
 namespace sk {
-
-namespace {
-constexpr int kWarps = 8;
-constexpr int kRowsPerWarp = 4;
-constexpr int kRowsPerCta = kWarps * kRowsPerWarp;  // 32: one lane per row in warp 0
-constexpr int kPrefetch = 4;                          // partial rows per row loaded up front
-constexpr int kMaxSplits = 32;
-}  // namespace
-
-template <typename TO, int DV>
-__global__ void __launch_bounds__(kWarps * 32)
-    combine_kernel(Problem p, const float *__restrict__ o_part, const float *__restrict__ lse_part,
-                   const int32_t *__restrict__ counts, TensorView out, float *__restrict__ lse_out,
-                   int row_blocks) {
-    static_assert(DV % 4 == 0 && DV / 4 <= 32, "one float4 per lane");
-    constexpr int kLanes = DV / 4;
-    __shared__ float sW[kMaxSplits][kRowsPerCta];
-    __shared__ float sInv[kRowsPerCta];
-    ptx::wait_prior_grid();  // launched early (programmatic serialization): partials complete
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int h = blockIdx.y;
-    const int b = blockIdx.x / row_blocks;
-    const int pos0 = (blockIdx.x % row_blocks) * kRowsPerCta;
-    const SeqInfo si = seq_info(p, b);
-    if (pos0 >= si.sq) return;
-    const int nrows = min(kRowsPerCta, si.sq - pos0);
-    const int S = p.S;
-    const int64_t plane = (int64_t)p.total_q;          // rows per (head, split) plane
-    const int row0 = si.q0 + pos0;
-    const float *obase = o_part + ((int64_t)h * S * plane + row0) * DV + lane * 4;
-
-    // ---- issue this warp's partial-row loads (they depend only on the counts)
-    int cnt[kRowsPerWarp];
-    float4 pre[kRowsPerWarp][kPrefetch];
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int r = warp * kRowsPerWarp + i;
-        cnt[i] = r < nrows ? merged_splits(p, si.sq, si.last_valid, pos0 + r, row_count(p, si, counts, pos0 + r)) : 0;
-    }
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int r = warp * kRowsPerWarp + i;
-#pragma unroll
-        for (int s = 0; s < kPrefetch; ++s)
-            pre[i][s] = (s < cnt[i] && lane < kLanes)
-                            ? __ldg((const float4 *)(obase + ((int64_t)s * plane + r) * DV))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-
-    // ---- weights: warp 0, one lane per row
-    if (warp == 0) {
-        const int r = lane;
-        const int c = r < nrows ? merged_splits(p, si.sq, si.last_valid, pos0 + r, row_count(p, si, counts, pos0 + r)) : 0;
-        const float *lrow = lse_part + (int64_t)h * S * plane + row0 + r;
-        float m = -FLT_MAX;  // max(max_s L_s, lowest finite)
-        for (int s = 0; s < c; ++s) {
-            const float l = __ldg(lrow + s * plane);
-            sW[s][r] = l;
-            m = fmaxf(m, l);
-        }
-        float wsum = 0.f;
-        for (int s = 0; s < c; ++s) {
-            const float w = expf(sW[s][r] - m);
-            sW[s][r] = w;
-            wsum += w;
-        }
-        sInv[r] = 1.f / fmaxf(wsum, 1.f);  // the max only binds when every split is empty
-        if (lse_out && r < nrows)
-            lse_out[(int64_t)h * plane + row0 + r] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
-    }
-    __syncthreads();
-
-    // ---- weighted sums and stores
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int r = warp * kRowsPerWarp + i;
-        if (r >= nrows) break;  // warp-uniform
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < kPrefetch; ++s) {
-            if (s < cnt[i]) {
-                const float w = sW[s][r];
-                acc.x = fmaf(w, pre[i][s].x, acc.x);
-                acc.y = fmaf(w, pre[i][s].y, acc.y);
-                acc.z = fmaf(w, pre[i][s].z, acc.z);
-                acc.w = fmaf(w, pre[i][s].w, acc.w);
-            }
-        }
-        for (int s = kPrefetch; s < cnt[i]; ++s) {  // more splits than prefetched
-            const float4 o = lane < kLanes
-                                 ? __ldg((const float4 *)(obase + ((int64_t)s * plane + r) * DV))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float w = sW[s][r];
-            acc.x = fmaf(w, o.x, acc.x);
-            acc.y = fmaf(w, o.y, acc.y);
-            acc.z = fmaf(w, o.z, acc.z);
-            acc.w = fmaf(w, o.w, acc.w);
-        }
-        const float inv = sInv[r];
-        if (lane < kLanes) {
-            TO *dst = (TO *)out.ptr + row_offset(p, out, b, si.q0, pos0 + r) + (int64_t)h * out.sh +
-                      lane * 4;
-            if constexpr (sizeof(TO) == 4) {
-                *(float4 *)dst = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            } else {
-                TO v[4] = {from_f32<TO>(acc.x * inv), from_f32<TO>(acc.y * inv),
-                           from_f32<TO>(acc.z * inv), from_f32<TO>(acc.w * inv)};
-                *(uint2 *)dst = *(const uint2 *)v;
-            }
-        }
-    }
-}
 
 // Launch with programmatic stream serialization: the combine's CTAs may be scheduled while
 // the partial kernel before it in the stream is finishing (it issues launch_dependents at
@@ -166,9 +46,9 @@ static cudaError_t launch_after_prior(void (*kern)(Params...), dim3 grid, dim3 b
 
 namespace {
 constexpr int kBulkThreads = 128;
-constexpr int kBulkRows = 16;  // packed rows per CTA (measured: 8 rows / 64 threads and
-                               // 32 rows / 256 threads no faster, 32 rows / 128 threads slower)
-constexpr int kBulkMaxSplits = 8;
+// Up to 8 splits: 16 packed rows per CTA (measured: 8 rows / 64 threads and 32 rows / 256
+// threads no faster, 32 rows / 128 threads slower); more splits take fewer rows, so that the
+// staged partials stay within 64 KB.
 constexpr uint64_t kBulkTimeoutNs = 1000000000ull;
 }  // namespace
 
@@ -196,7 +76,7 @@ __device__ inline int seq_of_row(const Problem &p, int row, int *pos) {
 // bulk copies before anything else is known; meanwhile warp 0 (one lane per row) loads
 // the row's S log-sum-exps, finds its sequence, count and weights. Splits that the
 // partition leaves empty are copied but never read (their memory may be unwritten).
-template <typename TO, int DV>
+template <typename TO, int DV, int kBulkRows, int kBulkMaxSplits>
 __global__ void __launch_bounds__(kBulkThreads)
     combine_bulk_kernel(Problem p, const float *__restrict__ o_part,
                         const float *__restrict__ lse_part, const int32_t *__restrict__ counts,
@@ -204,6 +84,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     static_assert(DV % 4 == 0 && DV / 4 <= 32, "one float4 per lane");
     constexpr int kLanes = DV / 4;
     constexpr int kRowsPerWarp = kBulkRows / (kBulkThreads / 32);
+    static_assert(kBulkRows % (kBulkThreads / 32) == 0 && kBulkRows <= 32, "rows per CTA");
     extern __shared__ __align__(128) uint8_t sO_raw[];   // [split][kBulkRows rows][DV] f32
     __shared__ __align__(8) uint64_t sBar;
     __shared__ float sW[kBulkMaxSplits][kBulkRows];
@@ -304,12 +185,13 @@ __global__ void __launch_bounds__(kBulkThreads)
     }
 }
 
-template <typename TO, int DV>
+template <typename TO, int DV, int ROWS, int MAXS>
 static cudaError_t launch_bulk(const Problem &p, const float *o_part, const float *lse_part,
                                const int32_t *counts, const TensorView &out, float *lse_out,
                                cudaStream_t st) {
-    auto kern = combine_bulk_kernel<TO, DV>;
-    constexpr int kMaxSmem = kBulkMaxSplits * kBulkRows * DV * 4;
+    auto kern = combine_bulk_kernel<TO, DV, ROWS, MAXS>;
+    constexpr int kMaxSmem = MAXS * ROWS * DV * 4;
+    static_assert(kMaxSmem <= 64 * 1024, "staged partials");
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
     int dev = 0;
@@ -318,31 +200,28 @@ static cudaError_t launch_bulk(const Problem &p, const float *o_part, const floa
         attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
-    const int row_blocks = (p.total_q + kBulkRows - 1) / kBulkRows;
-    const int smem = p.S * kBulkRows * DV * 4;
+    const int row_blocks = (p.total_q + ROWS - 1) / ROWS;
+    const int smem = p.S * ROWS * DV * 4;
     return launch_after_prior(kern, dim3((unsigned)row_blocks, (unsigned)p.H), dim3(kBulkThreads),
                               (size_t)smem, st, p, o_part, lse_part, counts, out, lse_out);
+}
+
+template <typename TO, int DV>
+static cudaError_t launch_splits(const Problem &p, const float *o_part, const float *lse_part,
+                                 const int32_t *counts, const TensorView &out, float *lse_out,
+                                 cudaStream_t st) {
+    if (p.S <= 8) return launch_bulk<TO, DV, 16, 8>(p, o_part, lse_part, counts, out, lse_out, st);
+    if (p.S <= 16) return launch_bulk<TO, DV, 8, 16>(p, o_part, lse_part, counts, out, lse_out, st);
+    if (p.S <= 32) return launch_bulk<TO, DV, 4, 32>(p, o_part, lse_part, counts, out, lse_out, st);
+    return cudaErrorInvalidValue;
 }
 
 template <typename TO>
 static cudaError_t launch_dv(const Problem &p, const float *o_part, const float *lse_part,
                              const int32_t *counts, const TensorView &out, float *lse_out,
                              cudaStream_t st) {
-    if (p.S > kMaxSplits) return cudaErrorInvalidValue;
-    if (p.S <= kBulkMaxSplits) {
-        if (p.d_v == 128) return launch_bulk<TO, 128>(p, o_part, lse_part, counts, out, lse_out, st);
-        if (p.d_v == 64) return launch_bulk<TO, 64>(p, o_part, lse_part, counts, out, lse_out, st);
-    }
-    const int row_blocks = (p.max_sq + kRowsPerCta - 1) / kRowsPerCta;
-    const long long nx = (long long)row_blocks * p.B;
-    if (nx > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    dim3 grid((unsigned)nx, (unsigned)p.H);
-    if (p.d_v == 128)
-        return launch_after_prior(combine_kernel<TO, 128>, grid, dim3(kWarps * 32), 0, st, p, o_part,
-                                  lse_part, counts, out, lse_out, row_blocks);
-    if (p.d_v == 64)
-        return launch_after_prior(combine_kernel<TO, 64>, grid, dim3(kWarps * 32), 0, st, p, o_part,
-                                  lse_part, counts, out, lse_out, row_blocks);
+    if (p.d_v == 128) return launch_splits<TO, 128>(p, o_part, lse_part, counts, out, lse_out, st);
+    if (p.d_v == 64) return launch_splits<TO, 64>(p, o_part, lse_part, counts, out, lse_out, st);
     return cudaErrorInvalidValue;
 }
 
