@@ -759,3 +759,26 @@ def test_random_problems_match_oracle(seed):
     counts = torch.empty(w.total_q, dtype=torch.int32, device=DEV)
     skv.sk_valid_split_counts(p, counts)
     assert np.array_equal(counts.cpu().numpy(), oracle.split_counts(H.oracle_problem(w, w.split_kv)))
+
+
+def test_persistent_form_beyond_its_unit_table():
+    """More than 16 rounds of units per CTA (40 sequences x 16 heads x 2 M blocks x split 4 =
+    5120 units on 152 CTAs): the rounds past the CTA's table are looked up as they come.
+    Sampled rows of every sequence against the oracle, and the partials of the last rows."""
+    rng = np.random.default_rng(47)
+    w = wl.Workload("persist many units", H=16,
+                    seqlens_q=tuple(int(x) for x in rng.integers(257, 400, 40)),
+                    seqlens_k=tuple(int(x) for x in rng.integers(300, 1200, 40)), d_qk=64, d_v=64,
+                    dtype="bf16", seed=47, n_per_block=64, split_kv=4, mask=wl.MASK_CAUSAL)
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    p = skv.params_for(w, DEV)
+    assert skv.sk_partial_kernel_name(p, qd, kd, vd) == "partial_tc_persist"
+    rows = H.sample_rows(w, head=4, tail=4, rand=4)
+    ref_o, ref_l = oracle.attention(H.oracle_problem(w, 1), q, k, v, rows=rows)
+    out, lse, _ = H.run_fwd(w, qd, kd, vd, DEV)
+    H.assert_close(H.to_np(out, rows), H.lse_np(lse, rows), ref_o, ref_l, w.dtype, "many units")
+    o_part, l_part, _ = H.run_partials(w, qd, kd, vd, DEV, 4)
+    tail = rows[-64:]
+    ref_po, ref_pl = oracle.partials(H.oracle_problem(w, 4), q, k, v, rows=tail)
+    H.assert_close(o_part.permute(2, 0, 1, 3).cpu().numpy()[tail], l_part.permute(2, 0, 1).cpu().numpy()[tail],
+                   ref_po, ref_pl, w.dtype, "many units partials")
