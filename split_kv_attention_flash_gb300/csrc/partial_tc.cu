@@ -55,14 +55,10 @@ constexpr int kThreads = 384;    // softmax warpgroups 0, 1; warpgroup 2: produc
 constexpr int kProducerWarp = 8;   // Q and K
 constexpr int kMmaWarp = 9;
 constexpr int kVProducerWarp = 10; // V
-// Registers are allocated per SM sub-partition: with 12 warps a thread may start with
-// at most 168. Warpgroup 2 gives registers back and the softmax warpgroups take them:
-// 2 * 128 * 208 + 128 * 88 = 384 * 168, exactly the launch's budget.
+// Every warp keeps the 168 registers a thread of a 12-warp CTA starts with. Moving some
+// of them from the control warps to the softmax warps made the MMA-issuing and producer
+// code spill while the softmax fits in 168; every long workload ran slower that way.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 208;
-constexpr int kControlRegs = 88;
-static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
-              "register split exceeds the launch budget");
 // Launches whose M blocks hold at most 128 queries split each block's key tiles between
 // the two halves (KVI), taking their (sequence, split) units longest first when there are
 // at most kLptMaxUnits of them and in index order otherwise. One query per sequence comes
@@ -292,7 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cb = dense ? b : 0;
 
     if (warp >= 8) {
-    ptx::regs_dec<kControlRegs>();
     if (warp == kProducerWarp || warp == kVProducerWarp) {
         // ---------------------------------------------------------- TMA producers
         // Two threads: K (with Q) and V, so that K(j + 1) is requested as soon as its
@@ -523,7 +518,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }  // warp 11 has no role
     } else {
         // ---------------------------------------------------------------- softmax
-        ptx::regs_inc<kSoftmaxRegs>();
         const int t = warp >> 2;
         const SoftmaxBars sb{bar(C::kBarS + t), bar(C::kBarP + t), bar(C::kBarO + t)};
         // epilogue staging: 4 KB per softmax warp in the K stages, which no load or MMA

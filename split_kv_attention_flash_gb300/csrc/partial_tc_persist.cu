@@ -49,11 +49,7 @@ constexpr int kPKWarp = 8;      // K producer
 constexpr int kPMmaWarp = 9;
 constexpr int kPVWarp = 10;     // V producer
 constexpr int kPQWarp = 11;     // Q producer
-constexpr int kPLaunchRegs = 168;
-constexpr int kPSoftmaxRegs = 208;
-constexpr int kPControlRegs = 88;
-static_assert(2 * 128 * kPSoftmaxRegs + 128 * kPControlRegs <= kPThreads * kPLaunchRegs,
-              "register split exceeds the launch budget");
+constexpr int kPLaunchRegs = 168;  // every warp keeps them (no reallocation, as in partial_tc)
 }  // namespace
 
 template <int DQK, int DV> struct PCfg {
@@ -213,7 +209,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const bool dense = p.cu_q == nullptr;
 
     if (warp >= 8) {
-        ptx::regs_dec<kPControlRegs>();
         if (lane == 0 && (warp == kPKWarp || warp == kPVWarp || warp == kPQWarp)) {
             // ---------------------------------------------------------- TMA producers
             int quiet = 0;
@@ -359,7 +354,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- softmax
-        ptx::regs_inc<kPSoftmaxRegs>();
         const int t = warp >> 2;
         const SoftmaxBars sb{bar(C::kBarS + t), bar(C::kBarP + t), bar(C::kBarO + t)};
         float4 *stage = (float4 *)(gen_base + (sStage - sQ)) + warp * 256;

@@ -169,14 +169,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool a_mn_major, boo
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Warpgroup register reallocation (all four warps of the warpgroup execute it).
-template <int N> __device__ __forceinline__ void regs_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N> __device__ __forceinline__ void regs_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ------------------------------------------------------------- conversions
 __device__ __forceinline__ float ex2(float x) {
     float y;
