@@ -154,8 +154,16 @@ WINDOW = TARGET_SHAPE.with_(name="sliding-window prefill bf16 Sq4096 Sk42700 H12
 DECODE_MQ = DECODE.with_(name="multi-query decode bf16 (B32 H32 Sq8, Sk ~ U[4096, 131072], D128)",
                          seqlens_q=(8,) * 32)
 
+# the masked workload under its prefix-causal mask: queries are the last 2048 positions of
+# the 4096 keys (prefix_offset = Sk - Sq), so rows past 952 reach the last valid key 3000 and
+# the splits beyond it hold no visible key
+MASKED_PREFIX_F16 = MASKED_F16.with_(
+    name="masked f16 prefix-causal (B1 H16 Sq2048 Sk4096 D128, offset 2048, BN64, S4, lastValid 3000)",
+    mask=MASK_PREFIX_CAUSAL, prefix_offset=2048)
+
 # a 4.3 GB decode case with the decode workload's layout (for profiler captures)
 DECODE_SMALL = DECODE.with_(name="decode bf16 (B32 H32 Sq1, Sk 8192, D128)", seqlens_k=(8192,) * 32)
 
 ALL = {"decode_small": DECODE_SMALL, "decode_mq": DECODE_MQ, "window": WINDOW, "tiny": TINY_CAUSAL, "noncausal": NONCAUSAL_BF16, "masked": MASKED_F16,
+       "masked_prefix": MASKED_PREFIX_F16,
        "varlen": LONG_VARLEN, "target": TARGET_SHAPE, "decode": DECODE, "target_d128": TARGET_D128}
