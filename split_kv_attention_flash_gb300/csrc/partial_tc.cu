@@ -365,13 +365,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tS[2] = {tmem, tmem + 128u};
             const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
             auto issue_qk = [&](int t, int j) {
-                const uint32_t kbase = sK + (j % C::kKStages) * C::kKBytes;
-                const uint32_t qbase = sQ + t * C::kQBytes;
+                const uint64_t kd = ptx::smem_desc_sw128(sK + (j % C::kKStages) * C::kKBytes, 16, 1024);
+                const uint64_t qd = ptx::smem_desc_sw128(sQ + t * C::kQBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < DQK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    ptx::mma_ss(tS[t], ptx::smem_desc_sw128(qbase + off, 16, 1024),
-                                ptx::smem_desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0);
+                    ptx::mma_ss(tS[t], ptx::desc_advance(qd, off), ptx::desc_advance(kd, off), kIdescQK, kk > 0);
                 }
                 ptx::tc_commit(bar(C::kBarS + t));
             };
@@ -379,12 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // spans the part's 64-column panels, kVPanelBytes apart
             auto issue_pv_part = [&](int t, int j, int hf) {
                 constexpr int kSteps = kBN / 16 / C::kVParts;
-                const uint32_t vbase = sV + (j % C::kVStages) * C::kVBytes + hf * C::kVPartBytes;
+                const uint64_t vd = ptx::smem_desc_sw128(sV + (j % C::kVStages) * C::kVBytes + hf * C::kVPartBytes,
+                                                         C::kVPanelBytes, 1024);
 #pragma unroll
                 for (int k4 = 0; k4 < kSteps; ++k4) {
                     const int kk = hf * kSteps + k4;
-                    ptx::mma_ts(tO[t], tS[t] + kk * 8,
-                                ptx::smem_desc_sw128(vbase + k4 * 2048, C::kVPanelBytes, 1024), kIdescPV,
+                    ptx::mma_ts(tO[t], tS[t] + kk * 8, ptx::desc_advance(vd, k4 * 2048), kIdescPV,
                                 (j > 0 || kk > 0) ? 1u : 0u);
                 }
             };
@@ -396,12 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   abort_flag, p.err, kErrMma, kTimeoutNs);
                 };
                 auto issue_qk_k = [&](int t, int k) {
-                    const uint32_t kbase = sK + (k % C::kKStages) * C::kKBytes;
+                    const uint64_t kd = ptx::smem_desc_sw128(sK + (k % C::kKStages) * C::kKBytes, 16, 1024);
+                    const uint64_t qd = ptx::smem_desc_sw128(sQ, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < DQK / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                        ptx::mma_ss(tS[t], ptx::smem_desc_sw128(sQ + off, 16, 1024),
-                                    ptx::smem_desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0);
+                        ptx::mma_ss(tS[t], ptx::desc_advance(qd, off), ptx::desc_advance(kd, off), kIdescQK, kk > 0);
                     }
                     ptx::tc_commit(bar(C::kBarS + t));
                     ptx::tc_commit(bar(C::kBarKE + k % C::kKStages));  // only S_t(i) reads K(k)
@@ -416,13 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     p.err, kErrMma, kTimeoutNs))
                             return false;
                         ptx::tc_fence_after();
-                        const uint32_t vbase = sV + vs * C::kVBytes + hf * C::kVPartBytes;
+                        const uint64_t vd = ptx::smem_desc_sw128(sV + vs * C::kVBytes + hf * C::kVPartBytes,
+                                                                 C::kVPanelBytes, 1024);
 #pragma unroll
                         for (int k4 = 0; k4 < kSteps; ++k4) {
                             const int kk = hf * kSteps + k4;
-                            ptx::mma_ts(tO[t], tS[t] + kk * 8,
-                                        ptx::smem_desc_sw128(vbase + k4 * 2048, C::kVPanelBytes, 1024),
-                                        kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                            ptx::mma_ts(tO[t], tS[t] + kk * 8, ptx::desc_advance(vd, k4 * 2048), kIdescPV,
+                                        (i > 0 || kk > 0) ? 1u : 0u);
                         }
                         ptx::tc_commit(bar(C::kBarVE + C::kVParts * vs + hf));
                     }

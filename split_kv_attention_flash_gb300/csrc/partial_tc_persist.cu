@@ -285,22 +285,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 return ptx::mbar_wait_bounded(bar(b), parity, abort_flag, p.err, kErrMma, kTimeoutNs);
             };
             auto issue_qk = [&](int t, int ks) {
-                const uint32_t kbase = sK + ks * C::kKBytes;
-                const uint32_t qbase = sQ + t * C::kQBytes;
+                const uint64_t kd = ptx::smem_desc_sw128(sK + ks * C::kKBytes, 16, 1024);
+                const uint64_t qd = ptx::smem_desc_sw128(sQ + t * C::kQBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < DQK / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                    ptx::mma_ss(tS[t], ptx::smem_desc_sw128(qbase + off, 16, 1024),
-                                ptx::smem_desc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0);
+                    ptx::mma_ss(tS[t], ptx::desc_advance(qd, off), ptx::desc_advance(kd, off), kIdescQK, kk > 0);
                 }
                 ptx::tc_commit(bar(C::kBarS + t));
             };
             auto issue_pv = [&](int t, int vs, bool first) {
-                const uint32_t vbase = sV + vs * C::kVBytes;
+                const uint64_t vd = ptx::smem_desc_sw128(sV + vs * C::kVBytes, C::kVPanelBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    ptx::mma_ts(tO[t], tS[t] + kk * 8,
-                                ptx::smem_desc_sw128(vbase + kk * 2048, C::kVPanelBytes, 1024), kIdescPV,
+                    ptx::mma_ts(tO[t], tS[t] + kk * 8, ptx::desc_advance(vd, kk * 2048), kIdescPV,
                                 (!first || kk > 0) ? 1u : 0u);
             };
             for (int i = 0; ok; ++i) {

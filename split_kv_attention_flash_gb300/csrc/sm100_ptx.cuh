@@ -159,6 +159,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The descriptor of an address `bytes` (a multiple of 16) past the one `d` describes.
+// Shared-memory addresses stay below 2^18, so the 14-bit start-address field of the
+// sum never carries into the leading-dimension field.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) {
+    return d + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor of tcgen05.mma .kind::f16 with an f32 accumulator:
 // D format (bits 4-5) = 1 (f32); A / B format (7-9 / 10-12) = 0 f16, 1 bf16;
 // A / B major (15 / 16) = 0 K-major, 1 MN-major; N >> 3 (17-22); M >> 4 (24-28).
