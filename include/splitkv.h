@@ -250,8 +250,12 @@ int sk_default_block_m(int d_qk, int d_v, sk_dtype dtype);
 int sk_supported_head_dims(int d_qk, int d_v);
 
 /* Name of the kernel sk_attn_partial_fwd would launch for these parameters, for
- * logging and benchmarks; NULL when the call would be rejected. split_kv = 0 is
- * resolved as sk_auto_split_kv resolves it (reading the current device). */
+ * logging and benchmarks: "partial_tc" (tensor cores, one unit per CTA),
+ * "partial_tc_persist" (tensor cores, one CTA per SM taking many short units in turn),
+ * "partial_decode" (CUDA cores, few queries per sequence) or "partial_fma" (CUDA cores,
+ * f32 and the remaining cases); NULL when the call would be rejected. split_kv = 0 is
+ * resolved as sk_auto_split_kv resolves it (reading the current device). The string is
+ * static; the caller does not free it. */
 const char *sk_partial_kernel_name(const sk_params *p, sk_tensor q, sk_tensor k, sk_tensor v);
 
 /* Human-readable text of a status code. */
