@@ -197,10 +197,11 @@ __device__ __forceinline__ void merge_block(const Problem &p, const SeqInfo &si,
 }
 
 // LPT: the (sequence, split) units -- the slowest launch dimension -- are taken longest
-// first (lpt_unit). Only instantiated for single-M-block launches of at most kLptMaxUnits
-// units (decode-like shapes with a few queries per sequence), where ragged sequence lengths
-// would otherwise leave the longest sequences for the last wave; prefill launches, and
-// single-block launches with more units, keep the unit from blockIdx.
+// first (lpt_unit), for launches of at most kLptMaxUnits units where ragged sequence
+// lengths would otherwise leave the longest sequences for the last wave: single-M-block
+// launches (decode-like shapes with a few queries per sequence) and partials of several
+// sequences over more than one wave of CTAs (packed varlen prefill). Other launches keep
+// the unit from blockIdx.
 // KVI: the single-block form (see Cfg); DIRECT: split 1, the output written directly.
 template <typename T, int DQK, int DV, bool DIRECT, bool LPT = false, bool KVI = false>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -629,6 +630,8 @@ static cudaError_t launch_cfg(const Problem &p, const CUtensorMap &mq, const CUt
     return cudaGetLastError();
 }
 
+static int sm_count_of_device();
+
 // out without tickets: S == 1, the kernel writes the output directly. out with
 // tickets: partials, merged by the last CTA of each M block. No out: partials only.
 template <typename T, int DQK, int DV>
@@ -653,7 +656,14 @@ static cudaError_t launch_dims(const Problem &p, const CUtensorMap &mq, const CU
     if (!(out && tickets) && p.max_sq <= kTileM)  // too many units to rank: index order
         return launch_cfg<T, DQK, DV, false, false, true>(p, mq, mk, mv, o_part, lse_part, TensorView{},
                                                           nullptr, nullptr, st);
-    if (!(out && tickets) && p.max_sq <= kBM && units > 1 && units <= kLptMaxUnits)
+    // Several sequences over more than one wave of CTAs: with ragged lengths, index order
+    // leaves the units of the longest sequences for the last waves, so they go first
+    // (long varlen prefill: 4.73 -> 4.61 ms at split 3). Within one wave, or with one
+    // sequence, the ranking only delays each CTA's start.
+    const long long ctas = (long long)((p.max_sq + kBM - 1) / kBM) * p.H * units;
+    const int sms = sm_count_of_device();
+    const bool ragged_waves = p.B > 1 && sms > 0 && ctas > sms;
+    if (!(out && tickets) && units > 1 && units <= kLptMaxUnits && (p.max_sq <= kBM || ragged_waves))
         return launch_cfg<T, DQK, DV, false, true>(p, mq, mk, mv, o_part, lse_part, TensorView{}, nullptr,
                                                    nullptr, st);
     return launch_cfg<T, DQK, DV, false>(p, mq, mk, mv, o_part, lse_part, out ? *out : TensorView{},
