@@ -213,7 +213,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     ptx::launch_dependents();  // the combine may be scheduled onto SMs this grid leaves idle
 
-    const int mb = blockIdx.x, h = blockIdx.y;
+    // under causal masks the last M blocks of a sequence see the most keys: they go first,
+    // so that the short ones fill the last wave (single-block launches have one M block)
+    const int mb = (!KVI && p.causal) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+    const int h = blockIdx.y;
     int s, b;
     if constexpr (LPT) {
         __shared__ int lpt_found;

@@ -161,9 +161,15 @@ MASKED_PREFIX_F16 = MASKED_F16.with_(
     name="masked f16 prefix-causal (B1 H16 Sq2048 Sk4096 D128, offset 2048, BN64, S4, lastValid 3000)",
     mask=MASK_PREFIX_CAUSAL, prefix_offset=2048)
 
+# causal self-attention prefill (not one of the pages' workloads: the usual causal shape,
+# where later query blocks see more keys)
+CAUSAL_PREFILL = Workload("causal prefill bf16 (B1 H16 Sq=Sk=16384, D128)", H=16, seqlens_q=(16384,),
+                          seqlens_k=(16384,), d_qk=128, d_v=128, dtype="bf16", seed=5,
+                          n_per_block=128, split_kv=0, mask=MASK_CAUSAL)
+
 # a 4.3 GB decode case with the decode workload's layout (for profiler captures)
 DECODE_SMALL = DECODE.with_(name="decode bf16 (B32 H32 Sq1, Sk 8192, D128)", seqlens_k=(8192,) * 32)
 
 ALL = {"decode_small": DECODE_SMALL, "decode_mq": DECODE_MQ, "window": WINDOW, "tiny": TINY_CAUSAL, "noncausal": NONCAUSAL_BF16, "masked": MASKED_F16,
-       "masked_prefix": MASKED_PREFIX_F16,
+       "masked_prefix": MASKED_PREFIX_F16, "causal_prefill": CAUSAL_PREFILL,
        "varlen": LONG_VARLEN, "target": TARGET_SHAPE, "decode": DECODE, "target_d128": TARGET_D128}
