@@ -418,6 +418,20 @@ def test_config_long_varlen_full():
     _sampled_check(w, [0, 2, 3, 4, 5, 6, 7, 8], rows_kw=dict(head=16, tail=16, rand=16))
 
 
+def test_ragged_causal_prefill_over_many_waves():
+    """Three ragged sequences under a causal mask with far more CTAs than SMs (11 M blocks x
+    16 heads x 9 units): the tensor-core kernel takes the (sequence, split) units longest
+    first and each sequence's M blocks last-first. Sampled rows of every sequence against the
+    oracle, at the automatic split and at 3, plus the split counts bit for bit."""
+    w = wl.Workload("ragged causal prefill", H=16, seqlens_q=(1500, 700, 2600),
+                    seqlens_k=(1500, 700, 2600), d_qk=192, d_v=128, dtype="bf16", seed=71,
+                    n_per_block=128, split_kv=3, mask=wl.MASK_CAUSAL)
+    q, k, v = w.make_inputs(DEV)
+    assert skv.sk_partial_kernel_name(skv.params_for(w, DEV), q, k, v) == "partial_tc"
+    del q, k, v
+    _sampled_check(w, [0, 3], rows_kw=dict(head=32, tail=32, rand=64))
+
+
 def test_target_shape_full():
     """The benchmark's default workload in the launch it times: automatic split (3)."""
     w = wl.TARGET_SHAPE
